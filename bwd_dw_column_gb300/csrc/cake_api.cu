@@ -1,0 +1,506 @@
+// cake_api.cu -- the C ABI: argument validation, the GB300 window table that
+// picks a variant per (H, rows, weight dtype, mode), workspace layout, and
+// dispatch to the kernel launchers.  Host code only.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/cake_rmsnorm.h"
+#include "cake_launch.h"
+
+namespace cake {
+
+// ------------------------------------------------------------ smem attributes
+
+cudaError_t ensure_smem_attr(const void *kernel, size_t smem)
+{
+    static std::mutex mu;
+    static std::vector<std::pair<std::pair<int, const void *>, size_t>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> g(mu);
+    for (auto &d : done)
+        if (d.first.first == dev && d.first.second == kernel && d.second >= smem)
+            return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    for (auto &d : done)
+        if (d.first.first == dev && d.first.second == kernel) {
+            d.second = smem;
+            return cudaSuccess;
+        }
+    done.push_back({{dev, kernel}, smem});
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------- window table
+
+// GB300: 152 SMs.  The CTA count is derived from this constant, never from
+// the device, so the deterministic pair's partition -- and so its dw bits --
+// depend on the shape alone.
+constexpr int kSMs = 152;
+constexpr size_t kSmemPerSM = 220 * 1024; // budget for the rings of co-resident CTAs
+constexpr int kMaxThreads = 512;
+constexpr int kMaxStages = 16;
+
+struct RowLayout {
+    int vpt, W;
+};
+
+// The row layout fixes which thread owns which columns and therefore the
+// reduction order of every per-row sum: it depends on H alone, so dx, y and
+// rstd are the same bits whatever else the table picks.
+static RowLayout row_layout(int H)
+{
+    const int nvec = H / 8;
+    if (nvec <= 32)
+        return {1, 1};
+    if (nvec <= 64)
+        return {2, 1};
+    int vpt = 2;
+    int W = (nvec + 63) / 64;
+    while (W > 15) {
+        ++vpt;
+        W = (nvec + 32 * vpt - 1) / (32 * vpt);
+    }
+    return {vpt, W};
+}
+
+struct Plan {
+    RowLayout rl;
+    int groups, stages, ctas_per_sm, ctas;
+    uint32_t rows_per_cta;
+    size_t smem;
+    int single, dwm;
+};
+
+static size_t ring_smem(int ntens, int groups, int H, int stages)
+{
+    return (size_t)kMiscBytes + (size_t)stages * ntens * groups * H * 2;
+}
+
+// Per-H CTA shape: row groups (rows in flight) per CTA and CTAs per SM.
+static void cta_shape(int H, const RowLayout &rl, int &groups, int &ctas_per_sm)
+{
+    const int W = rl.W;
+    const int max_warps = (rl.vpt == 1 ? 576 : kMaxThreads) / 32 - 1; // consumer warps
+    (void)H;
+    if (W == 1) {
+        groups = 16;
+        ctas_per_sm = 3;
+    } else if (W <= 4) {
+        groups = 2;
+        ctas_per_sm = W <= 3 ? 4 : 3;
+    } else if (W <= 8) {
+        groups = 1;
+        ctas_per_sm = 3;
+    } else {
+        groups = 1;
+        ctas_per_sm = 2;
+    }
+    while (groups * W > max_warps && groups > 1)
+        --groups;
+}
+
+static Plan make_plan(int H, uint32_t rows, int ntens, int single, int dwm)
+{
+    Plan p;
+    p.rl = row_layout(H);
+    cta_shape(H, p.rl, p.groups, p.ctas_per_sm);
+    const size_t per_cta = kSmemPerSM / p.ctas_per_sm;
+    const size_t stage = (size_t)ntens * p.groups * H * 2;
+    int stages = (int)((per_cta - kMiscBytes) / stage);
+    if (stages > kMaxStages)
+        stages = kMaxStages;
+    if (stages < 2) { // fewer CTAs per SM so that at least two stages fit
+        p.ctas_per_sm = 1;
+        stages = (int)((kSmemPerSM - kMiscBytes) / stage);
+        if (stages > kMaxStages)
+            stages = kMaxStages;
+    }
+    p.stages = stages;
+    p.smem = ring_smem(ntens, p.groups, H, stages);
+    // the group-combine buffer reuses the ring
+    const size_t comb = (size_t)kMiscBytes + (size_t)(p.groups > 1 ? p.groups - 1 : 0) * H * 8;
+    if (comb > p.smem)
+        p.smem = comb;
+    const uint32_t tile = (uint32_t)p.groups;
+    const uint32_t max_ctas = (uint32_t)kSMs * p.ctas_per_sm;
+    uint32_t ctas = rows == 0 ? 0 : (rows + tile - 1) / tile; // at least one tile per CTA
+    if (ctas > max_ctas)
+        ctas = max_ctas;
+    p.rows_per_cta = ctas ? (rows + ctas - 1) / ctas : 0;
+    p.ctas = p.rows_per_cta ? (int)((rows + p.rows_per_cta - 1) / p.rows_per_cta) : 0;
+    p.single = single;
+    p.dwm = dwm;
+    return p;
+}
+
+// Mode / accumulation choice.  Deterministic: the pair.  Non-deterministic:
+// the single kernel (FP64 column accumulation).  The per-thread accumulation
+// is the compensated TwoSum form; small row counts (a few rows per thread)
+// take the plain FP32 sum, whose error there is far inside the budget.
+static void pick_variant(uint32_t rows, int deterministic, int &single, int &dwm)
+{
+    single = deterministic ? 0 : 1;
+    dwm = rows <= 2048 ? CAKE_DW_PLAIN : CAKE_DW_TWOSUM;
+}
+
+// ---------------------------------------------------------- workspace layout
+
+constexpr size_t kWsHeader = 256; // arrival counter (+ padding)
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static size_t ws_acc_off() { return kWsHeader; }
+static size_t ws_part_off(int H) { return align256(kWsHeader + (size_t)H * 8); }
+static size_t ws_size(int H, int ctas, int need_partials)
+{
+    return ws_part_off(H) + (need_partials ? (size_t)ctas * H * 8 : 0);
+}
+
+} // namespace cake
+
+using namespace cake;
+
+// ------------------------------------------------------------- validation
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cake_status check_shape(const cake_shape *s, uint32_t *rows)
+{
+    if (!s || s->tokens < 0 || s->heads < 1 || s->hidden < 1)
+        return CAKE_ERR_INVALID;
+    if (s->hidden % 8 != 0 || s->hidden > CAKE_MAX_HIDDEN)
+        return CAKE_ERR_UNSUPPORTED;
+    const int64_t r = s->tokens * s->heads;
+    if (s->tokens > 0 && r / s->tokens != s->heads)
+        return CAKE_ERR_UNSUPPORTED;
+    if (r >= (int64_t(1) << 31))
+        return CAKE_ERR_UNSUPPORTED;
+    *rows = (uint32_t)r;
+    return CAKE_OK;
+}
+
+// Activation tensor: non-null, 16-byte aligned base, strides multiples of 8
+// elements (16 bytes) and non-negative.
+cake_status check_tensor(const cake_tensor *t, const cake_shape *s)
+{
+    if (!t || !t->data)
+        return CAKE_ERR_INVALID;
+    if (t->stride_token < 0 || t->stride_head < 0)
+        return CAKE_ERR_UNSUPPORTED;
+    if (!aligned16(t->data) || t->stride_token % 8 != 0 ||
+        (s->heads > 1 && t->stride_head % 8 != 0))
+        return CAKE_ERR_UNSUPPORTED;
+    if (s->tokens > 1 && t->stride_token < (s->heads > 1 ? 0 : s->hidden))
+        return CAKE_ERR_UNSUPPORTED;
+    if (s->heads > 1 && t->stride_head < s->hidden)
+        return CAKE_ERR_UNSUPPORTED;
+    return CAKE_OK;
+}
+
+RowView make_view(const cake_tensor *t, const cake_shape *s)
+{
+    RowView v{};
+    if (!t || !t->data)
+        return v;
+    v.base = static_cast<const uint16_t *>(t->data);
+    v.st = t->stride_token;
+    v.sh = s->heads > 1 ? t->stride_head : 0;
+    if (s->heads == 1) {
+        v.uniform = 1;
+        v.row_stride = t->stride_token;
+    } else if (t->stride_token == s->heads * t->stride_head) {
+        v.uniform = 1;
+        v.row_stride = t->stride_head;
+    } else if (s->tokens == 1) {
+        v.uniform = 1;
+        v.row_stride = t->stride_head;
+    }
+    v.dense = v.uniform && v.row_stride == s->hidden;
+    return v;
+}
+
+cake_status cuda_status(cudaError_t e)
+{
+    return e == cudaSuccess ? CAKE_OK : CAKE_ERR_CUDA;
+}
+
+Layout make_layout(const Plan &p, int H, uint32_t rows, uint32_t nh, int ntens)
+{
+    Layout L;
+    L.H = H;
+    L.nvec = H / 8;
+    L.warps_per_row = p.rl.W;
+    L.groups = p.groups;
+    L.stages = p.stages;
+    L.ntens = ntens;
+    L.rows = rows;
+    L.nh = nh;
+    L.rows_per_cta = p.rows_per_cta;
+    L.inv_h = 1.0f / (float)H;
+    return L;
+}
+
+void fill_variant(const Plan &p, cake_variant *out)
+{
+    out->single = p.single;
+    out->dw_accum = p.dwm;
+    out->vec_per_thread = p.rl.vpt;
+    out->warps_per_row = p.rl.W;
+    out->row_groups = p.groups;
+    out->stages = p.stages;
+    out->ctas = p.ctas;
+    out->rows_per_cta = p.rows_per_cta;
+    out->smem_bytes = p.smem;
+}
+
+cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, int force_single,
+                        int force_accum, Plan *plan, uint32_t *rows)
+{
+    cake_status st = check_shape(shape, rows);
+    if (st != CAKE_OK)
+        return st;
+    if (force_single > 1 || force_accum > CAKE_DW_TWOSUM)
+        return CAKE_ERR_INVALID;
+    if (deterministic && force_single == 1)
+        return CAKE_ERR_INVALID;
+    int single, dwm;
+    pick_variant(*rows, deterministic, single, dwm);
+    if (force_single >= 0)
+        single = force_single;
+    if (force_accum >= 0)
+        dwm = force_accum;
+    *plan = make_plan((int)shape->hidden, *rows, has_dh ? 3 : 2, single, dwm);
+    return CAKE_OK;
+}
+
+cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_tensor *x,
+                    const float *rstd, const void *w, cake_dtype w_dtype, const cake_tensor *dh,
+                    const cake_tensor *dx, float *dw, void *workspace, size_t workspace_bytes,
+                    int deterministic, int force_single, int force_accum, cake_stream_t stream)
+{
+    uint32_t rows = 0;
+    const int has_dh = dh && dh->data;
+    Plan plan;
+    cake_status st = select_plan(shape, deterministic, has_dh, force_single, force_accum, &plan, &rows);
+    if (st != CAKE_OK)
+        return st;
+    if (w_dtype != CAKE_BF16 && w_dtype != CAKE_FP32)
+        return CAKE_ERR_INVALID;
+    if (!dw || !w)
+        return CAKE_ERR_INVALID;
+    if (!aligned16(w) || !aligned16(dw))
+        return CAKE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int H = (int)shape->hidden;
+    if (rows == 0)
+        return cuda_status(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), s));
+    if (!rstd)
+        return CAKE_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(rstd) & 3u) != 0)
+        return CAKE_ERR_UNSUPPORTED;
+    if ((st = check_tensor(dy, shape)) != CAKE_OK || (st = check_tensor(x, shape)) != CAKE_OK ||
+        (st = check_tensor(dx, shape)) != CAKE_OK)
+        return st;
+    if (has_dh && (st = check_tensor(dh, shape)) != CAKE_OK)
+        return st;
+    const size_t need = ws_size(H, plan.ctas, !plan.single);
+    if (!workspace || workspace_bytes < need)
+        return CAKE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return CAKE_ERR_UNSUPPORTED;
+
+    BwdParams p{};
+    p.L = make_layout(plan, H, rows, (uint32_t)shape->heads, has_dh ? 3 : 2);
+    p.x = make_view(x, shape);
+    p.dy = make_view(dy, shape);
+    p.dh = make_view(has_dh ? dh : nullptr, shape);
+    p.rstd = rstd;
+    p.w = w;
+    p.w_f32 = w_dtype == CAKE_FP32;
+    RowView dxv = make_view(dx, shape);
+    p.dx = static_cast<uint16_t *>(dx->data);
+    p.dx_st = dxv.st;
+    p.dx_sh = dxv.sh;
+    p.dx_row_stride = dxv.row_stride;
+    p.dx_uniform = dxv.uniform;
+    p.dw = dw;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.arrivals = reinterpret_cast<unsigned int *>(ws);
+    p.acc = reinterpret_cast<double *>(ws + ws_acc_off());
+    p.partials = reinterpret_cast<float2 *>(ws + ws_part_off(H));
+    p.block_rows = 16;
+    p.status = nullptr;
+    return cuda_status(launch_bwd(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s));
+}
+
+} // namespace
+
+// ------------------------------------------------------------------- C ABI
+
+extern "C" {
+
+int cake_rmsnorm_abi_version(void) { return CAKE_ABI_VERSION; }
+
+const char *cake_status_str(cake_status status)
+{
+    switch (status) {
+    case CAKE_OK: return "ok";
+    case CAKE_ERR_INVALID: return "invalid argument";
+    case CAKE_ERR_UNSUPPORTED: return "unsupported shape, stride or alignment";
+    case CAKE_ERR_WORKSPACE: return "workspace missing or too small";
+    case CAKE_ERR_CUDA: return "CUDA runtime error";
+    case CAKE_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    }
+    return "unknown status";
+}
+
+cake_status cake_rmsnorm_fwd(const cake_shape *shape, const cake_tensor *x,
+                             const cake_tensor *residual, const void *w, cake_dtype w_dtype,
+                             float eps, const cake_tensor *y, const cake_tensor *h_new,
+                             float *rstd, cake_stream_t stream)
+{
+    uint32_t rows = 0;
+    cake_status st = check_shape(shape, &rows);
+    if (st != CAKE_OK)
+        return st;
+    if (w_dtype != CAKE_BF16 && w_dtype != CAKE_FP32)
+        return CAKE_ERR_INVALID;
+    if (!(eps >= 0.0f))
+        return CAKE_ERR_INVALID;
+    const int has_res = residual && residual->data;
+    if (rows == 0)
+        return CAKE_OK;
+    if (!w || !rstd)
+        return CAKE_ERR_INVALID;
+    if (!aligned16(w) || (reinterpret_cast<uintptr_t>(rstd) & 3u) != 0)
+        return CAKE_ERR_UNSUPPORTED;
+    if ((st = check_tensor(x, shape)) != CAKE_OK || (st = check_tensor(y, shape)) != CAKE_OK)
+        return st;
+    if (has_res) {
+        if ((st = check_tensor(residual, shape)) != CAKE_OK || (st = check_tensor(h_new, shape)) != CAKE_OK)
+            return st;
+    } else if (h_new && h_new->data) {
+        return CAKE_ERR_INVALID;
+    }
+    const int H = (int)shape->hidden;
+    const int ntens = has_res ? 2 : 1;
+    Plan plan = make_plan(H, rows, ntens, 0, 0);
+    FwdParams p{};
+    p.L = make_layout(plan, H, rows, (uint32_t)shape->heads, ntens);
+    p.x = make_view(x, shape);
+    p.res = make_view(has_res ? residual : nullptr, shape);
+    p.w = w;
+    p.w_f32 = w_dtype == CAKE_FP32;
+    p.eps = eps;
+    RowView yv = make_view(y, shape);
+    p.y = static_cast<uint16_t *>(y->data);
+    p.y_st = yv.st;
+    p.y_sh = yv.sh;
+    p.y_row_stride = yv.row_stride;
+    p.y_uniform = yv.uniform;
+    if (has_res) {
+        RowView hv = make_view(h_new, shape);
+        p.h_new = static_cast<uint16_t *>(h_new->data);
+        p.hn_st = hv.st;
+        p.hn_sh = hv.sh;
+        p.hn_row_stride = hv.row_stride;
+        p.hn_uniform = hv.uniform;
+    }
+    p.rstd = rstd;
+    p.status = nullptr;
+    return cuda_status(launch_fwd(p, plan.rl.vpt, plan.ctas, plan.smem,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t cake_rmsnorm_bwd_workspace_size(const cake_shape *shape, cake_dtype w_dtype, int deterministic)
+{
+    (void)w_dtype;
+    uint32_t rows = 0;
+    if (check_shape(shape, &rows) != CAKE_OK || rows == 0)
+        return 0;
+    // the largest of every variant this mode may run (the table or a forced one)
+    const int H = (int)shape->hidden;
+    size_t need = 0;
+    for (int ntens = 2; ntens <= 3; ++ntens) {
+        Plan p = make_plan(H, rows, ntens, 0, 0);
+        size_t n = ws_size(H, p.ctas, 1);
+        if (n > need)
+            need = n;
+    }
+    (void)deterministic;
+    return need;
+}
+
+cake_status cake_rmsnorm_bwd_workspace_init(void *workspace, size_t workspace_bytes, cake_stream_t stream)
+{
+    if (!workspace && workspace_bytes)
+        return CAKE_ERR_INVALID;
+    if (!workspace_bytes)
+        return CAKE_OK;
+    return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+cake_status cake_rmsnorm_bwd_select(const cake_shape *shape, cake_dtype w_dtype, int deterministic,
+                                    int has_dh, int force_single, int force_accum, cake_variant *out)
+{
+    if (!out)
+        return CAKE_ERR_INVALID;
+    if (w_dtype != CAKE_BF16 && w_dtype != CAKE_FP32)
+        return CAKE_ERR_INVALID;
+    Plan plan;
+    uint32_t rows = 0;
+    cake_status st = select_plan(shape, deterministic, has_dh, force_single, force_accum, &plan, &rows);
+    if (st != CAKE_OK)
+        return st;
+    fill_variant(plan, out);
+    return CAKE_OK;
+}
+
+cake_status cake_rmsnorm_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_tensor *x,
+                             const float *rstd, const void *w, cake_dtype w_dtype,
+                             const cake_tensor *dh, const cake_tensor *dx, float *dw,
+                             void *workspace, size_t workspace_bytes, int deterministic,
+                             cake_stream_t stream)
+{
+    return run_bwd(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, workspace, workspace_bytes,
+                   deterministic, -1, -1, stream);
+}
+
+cake_status cake_rmsnorm_bwd_forced(const cake_shape *shape, const cake_tensor *dy,
+                                    const cake_tensor *x, const float *rstd, const void *w,
+                                    cake_dtype w_dtype, const cake_tensor *dh, const cake_tensor *dx,
+                                    float *dw, void *workspace, size_t workspace_bytes,
+                                    int deterministic, int force_single, int force_accum,
+                                    cake_stream_t stream)
+{
+    return run_bwd(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, workspace, workspace_bytes,
+                   deterministic, force_single, force_accum, stream);
+}
+
+cake_status cake_rmsnorm_device_status(int *code, int clear)
+{
+    if (!code)
+        return CAKE_ERR_INVALID;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return CAKE_ERR_CUDA;
+    int a = 0, b = 0;
+    if (fwd_status(&a, clear) != cudaSuccess || bwd_status(&b, clear) != cudaSuccess)
+        return CAKE_ERR_CUDA;
+    *code = a ? a : b;
+    return CAKE_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,21 @@
+// cake_launch.h -- private interface between the C ABI (cake_api.cu) and the
+// kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "cake_params.h"
+
+namespace cake {
+
+// Raise a kernel's dynamic shared memory limit once per (device, kernel).
+cudaError_t ensure_smem_attr(const void *kernel, size_t smem);
+
+cudaError_t launch_fwd(const FwdParams &p, int vpt, int ctas, size_t smem, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
+                       cudaStream_t stream);
+
+cudaError_t fwd_status(int *code, int clear);
+cudaError_t bwd_status(int *code, int clear);
+
+} // namespace cake

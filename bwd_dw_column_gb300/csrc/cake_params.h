@@ -1,0 +1,81 @@
+// cake_params.h -- launch parameters shared by the host launchers and the
+// kernels (plain structs, passed by value as __grid_constant__ arguments).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace cake {
+
+// Bytes at the start of a CTA's dynamic shared memory for the mbarriers, the
+// per-row reduction slots and flags; the staging ring follows.
+constexpr int kMiscBytes = 1024;
+
+// A BF16 [T, nh, H] view.  Row r = (t, k) = (r / nh, r % nh) starts at
+// base + t*st + k*sh (elements).  When the rows are equally spaced
+// (nh == 1, or st == nh*sh) `uniform` is set and row r is at base + r*row_stride.
+struct RowView {
+    const uint16_t *base;
+    int64_t st, sh;
+    int64_t row_stride;
+    int uniform;
+    int dense; // uniform and row_stride == H: a run of rows is one contiguous block
+};
+
+// How a CTA is organised, shared by all kernels of the row pipeline.
+//   consumer warps = groups * warps_per_row; one extra producer warp issues the
+//   bulk copies.  A pipeline stage holds `groups` rows (one per group) of each
+//   staged tensor.
+struct Layout {
+    int H;              // elements per row
+    int nvec;           // H / 8: 16-byte vectors per row
+    int warps_per_row;  // W
+    int groups;         // NG
+    int stages;         // ring depth
+    int ntens;          // tensors staged per row (x[, residual] / x, dy[, dh])
+    uint32_t rows;      // total rows R = T * nh
+    uint32_t nh;
+    uint32_t rows_per_cta; // contiguous rows per CTA (the last CTA may own fewer)
+    float inv_h;        // 1.0f / H
+};
+
+struct FwdParams {
+    Layout L;
+    RowView x, res;     // res.base == nullptr: plain rows
+    const void *w;      // [H] BF16 or FP32
+    int w_f32;
+    float eps;
+    uint16_t *y;
+    int64_t y_st, y_sh, y_row_stride;
+    int y_uniform;
+    uint16_t *h_new;
+    int64_t hn_st, hn_sh, hn_row_stride;
+    int hn_uniform;
+    float *rstd;
+    int *status;
+};
+
+struct BwdParams {
+    Layout L;
+    RowView x, dy, dh;  // staged tensors; dh.base == nullptr: no dh
+    const float *rstd;
+    const void *w;
+    int w_f32;
+    uint16_t *dx;
+    int64_t dx_st, dx_sh, dx_row_stride;
+    int dx_uniform;
+    float *dw;          // [H]
+    float2 *partials;   // pair: [ctas][H] (hi, lo)
+    double *acc;        // single: [H] FP64 column accumulators (zero between calls)
+    unsigned int *arrivals; // single: CTA arrival counter (zero between calls)
+    int block_rows;     // blocked accumulation: rows per FP32 block
+    int *status;
+};
+
+struct ReduceParams {
+    const float2 *partials; // [P][H]
+    int P, H;
+    float *dw;
+};
+
+} // namespace cake

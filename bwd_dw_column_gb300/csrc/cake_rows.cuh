@@ -1,0 +1,202 @@
+// cake_rows.cuh -- the row pipeline shared by the forward and backward kernels.
+//
+// CTA organisation (all kernels of this library that stream rows):
+//   * warps [0, groups*W) are consumers; a "row group" of W warps owns one row
+//     at a time, each thread holding VPT 16-byte vectors of that row in
+//     registers (vector v = k*32*W + thread-in-group, k < VPT);
+//   * the last warp is the producer: it streams the CTA's contiguous chunk of
+//     rows into a `stages`-deep shared-memory ring with cp.async.bulk copies
+//     (one per row, or one per stage when the rows are dense) that complete on
+//     the stage's `full` mbarrier; consumers release a stage on its `empty`
+//     mbarrier (one arrival per consumer warp);
+//   * the per-row reductions (sum of squares, sum of g*xhat) are a warp
+//     butterfly plus, when W > 1, a fixed-order sum of the W warp partials
+//     through shared memory behind one named barrier per row.
+// No CTA ever waits on another CTA.  Every mbarrier wait is bounded
+// (kWaitLimitNs); a wait that runs out sets the status word to
+// CAKE_ERR_TIMEOUT and the CTA leaves its loop after draining its own copies.
+#pragma once
+
+#include "cake_device.cuh"
+
+namespace cake {
+
+constexpr int kStatusTimeout = 5; // == CAKE_ERR_TIMEOUT
+constexpr int kConsumerBarrier = 9;
+
+struct Smem {
+    uint64_t *full;   // [stages]
+    uint64_t *empty;  // [stages]
+    float *red;       // [groups][2][W]
+    int *flag;        // [4]
+    uint8_t *ring;    // stages * stage_bytes
+    uint32_t stage_bytes;
+    uint32_t tens_bytes; // bytes of one tensor in one stage
+};
+
+__device__ __forceinline__ Smem carve_smem(uint8_t *base, const Layout &L)
+{
+    Smem s;
+    s.full = reinterpret_cast<uint64_t *>(base);
+    s.empty = s.full + L.stages;
+    s.red = reinterpret_cast<float *>(base + 16 * 2 * 8);
+    s.flag = reinterpret_cast<int *>(base + kMiscBytes - 16);
+    s.ring = base + kMiscBytes;
+    s.tens_bytes = (uint32_t)L.groups * L.H * 2;
+    s.stage_bytes = s.tens_bytes * L.ntens;
+    return s;
+}
+
+// Thread 0 initialises the ring's barriers; everyone syncs once.
+__device__ __forceinline__ void init_ring(const Smem &s, const Layout &L)
+{
+    if (threadIdx.x == 0) {
+        const int consumer_warps = L.groups * L.warps_per_row;
+        for (int i = 0; i < L.stages; ++i) {
+            mbar_init(smem_addr(&s.full[i]), 1);
+            mbar_init(smem_addr(&s.empty[i]), consumer_warps);
+        }
+        s.flag[0] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+}
+
+struct Chunk {
+    uint32_t r0, r_end, ntiles, tile_rows;
+};
+
+__device__ __forceinline__ Chunk cta_chunk(const Layout &L)
+{
+    Chunk c;
+    c.r0 = blockIdx.x * L.rows_per_cta;
+    uint32_t e = c.r0 + L.rows_per_cta;
+    c.r_end = e < L.rows ? e : L.rows;
+    c.tile_rows = (uint32_t)L.groups;
+    c.ntiles = c.r_end > c.r0 ? (c.r_end - c.r0 + c.tile_rows - 1) / c.tile_rows : 0;
+    return c;
+}
+
+// Producer warp: stream `ntens` tensors of the chunk into the ring.
+// views[i] is the i-th staged tensor.  Returns false on a timeout.
+template <int NT>
+__device__ __forceinline__ void produce(const Smem &s, const Layout &L, const Chunk &c,
+                                       const RowView (&views)[NT], int ntens, int *status)
+{
+    const int lane = threadIdx.x & 31;
+    const uint64_t pol = policy_evict_first();
+    const uint32_t row_bytes = (uint32_t)L.H * 2;
+    bool ok = true;
+    uint32_t it = 0;
+    for (; it < c.ntiles; ++it) {
+        const uint32_t st = it % L.stages;
+        if (it >= (uint32_t)L.stages) {
+            const uint32_t par = ((it / L.stages) - 1) & 1;
+            bool got = mbar_wait(smem_addr(&s.empty[st]), par);
+            got = __all_sync(0xffffffffu, got);
+            if (!got) {
+                if (lane == 0)
+                    set_status(status, kStatusTimeout);
+                ok = false;
+                break;
+            }
+        }
+        const uint32_t row0 = c.r0 + it * c.tile_rows;
+        const uint32_t left = c.r_end - row0;
+        const uint32_t n = left < c.tile_rows ? left : c.tile_rows;
+        const uint32_t full_bar = smem_addr(&s.full[st]);
+        if (lane == 0)
+            mbar_arrive_expect_tx(full_bar, (uint32_t)ntens * n * row_bytes);
+        __syncwarp();
+        const uint32_t stage_base = smem_addr(s.ring) + st * s.stage_bytes;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t >= ntens)
+                break;
+            const RowView &v = views[t];
+            const uint32_t dst = stage_base + t * s.tens_bytes;
+            if (v.dense) {
+                if (lane == 0)
+                    bulk_g2s(dst, v.base + (int64_t)row0 * v.row_stride, n * row_bytes, full_bar, pol);
+            } else {
+                for (uint32_t q = lane; q < n; q += 32)
+                    bulk_g2s(dst + q * row_bytes, v.base + row_off(v, row0 + q, L.nh), row_bytes,
+                             full_bar, pol);
+            }
+        }
+    }
+    // Never leave copies in flight: wait (bounded) for the last issued stages.
+    const uint32_t issued = it;
+    const uint32_t first = issued > (uint32_t)L.stages ? issued - L.stages : 0;
+    for (uint32_t j = first; j < issued; ++j) {
+        if (!mbar_wait(smem_addr(&s.full[j % L.stages]), (j / L.stages) & 1)) {
+            if (lane == 0)
+                set_status(status, kStatusTimeout);
+        }
+    }
+    (void)ok;
+}
+
+// Per-row group reduction: warp butterfly, then (W > 1) a fixed-order sum of
+// the W warp partials.  `abort` is OR-ed across the group.  `slot` toggles
+// per row so one barrier per row suffices.
+__device__ __forceinline__ float group_sum(float v, const Smem &s, const Layout &L, int gid,
+                                           int wig, int lane, uint32_t slot, bool &abort)
+{
+    v = warp_sum(v);
+    const int W = L.warps_per_row;
+    if (W == 1) {
+        abort = __any_sync(0xffffffffu, abort);
+        return v;
+    }
+    float *red = s.red + (gid * 2 + (slot & 1)) * W;
+    if (lane == 0)
+        red[wig] = v;
+    abort = named_sync_or(1 + gid, 32 * W, abort);
+    float t = 0.f;
+    for (int w = 0; w < W; ++w)
+        t += red[w];
+    return t;
+}
+
+__device__ __forceinline__ void consumer_sync(const Layout &L)
+{
+    named_sync(kConsumerBarrier, 32 * L.groups * L.warps_per_row);
+}
+
+// Load this thread's VPT vectors of w as FP32 (zeros past the row end).
+template <int VPT>
+__device__ __forceinline__ void load_weight(const void *w, int w_f32, int nvec, int gtid, int W,
+                                            float (&wf)[VPT][8])
+{
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * 32 * W + gtid;
+        if (v < nvec) {
+            if (w_f32) {
+                const float4 *p = reinterpret_cast<const float4 *>(w) + 2 * v;
+                float4 a = p[0], b = p[1];
+                wf[k][0] = a.x; wf[k][1] = a.y; wf[k][2] = a.z; wf[k][3] = a.w;
+                wf[k][4] = b.x; wf[k][5] = b.y; wf[k][6] = b.z; wf[k][7] = b.w;
+            } else {
+                uint4 u = reinterpret_cast<const uint4 *>(w)[v];
+                unpack8(u, wf[k]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                wf[k][e] = 0.f;
+        }
+    }
+}
+
+__device__ __forceinline__ int64_t out_off(int64_t st, int64_t sh, int64_t row_stride, int uniform,
+                                           uint32_t r, uint32_t nh)
+{
+    if (uniform)
+        return (int64_t)r * row_stride;
+    const uint32_t t = r / nh, k = r - t * nh;
+    return (int64_t)t * st + (int64_t)k * sh;
+}
+
+} // namespace cake

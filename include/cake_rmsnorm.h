@@ -1,0 +1,208 @@
+/*
+ * cake_rmsnorm.h -- C ABI of a training RMSNorm for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (the pages give names, dtypes and shapes, not formulas; the
+ * formulas below are the standard RMSNorm and its exact gradient):
+ *
+ *   forward   h     = x                     (plain rows), or
+ *             h     = bf16(x + residual)    (fused residual add; h is also
+ *                                            returned as h_new)
+ *             rstd  = 1 / sqrt(mean_j(h_j^2) + eps)        FP32, per row
+ *             y_j   = bf16(h_j * rstd * w_j)
+ *   backward  g_j   = dy_j * w_j,  xhat_j = h_j * rstd,  c = mean_j(g_j * xhat_j)
+ *             dx_j  = bf16(rstd * (g_j - xhat_j * c) [+ dh_j])
+ *             dw_j  = sum over all rows of dy_j * h_j * rstd      FP32
+ *
+ * Sources (page title, then the part of the page):
+ *   - outputs and dtypes (y/dx BF16, rstd/dw FP32), the two backward modes
+ *     sharing one forward, the per-head views and the `res` / `w32` routes:
+ *     "Speedups ... GB300 windows" commit (#8577) quoted on the page of
+ *     "feat(cake_rmsnorm): opt-in non-deterministic weight gradient for the
+ *     autograd RMSNorm - #8208", intro and "Key"; PR #8899 page, first
+ *     paragraph.
+ *   - `deterministic` (default true): true gives a dw that is bitwise
+ *     reproducible, false allows a single-kernel form whose dw is not; dx is
+ *     bitwise identical across calls in both modes: #8208 page, description.
+ *   - the deterministic backward is a pair: a main kernel that writes
+ *     CTA-partial dw into a workspace, then a fixed-order dw reduce: #8577
+ *     commit, intro; the workspace entry points: #8208 page, description.
+ *   - per-head views: query [T, 24, 256] with strides (12288, 512, 1) and key
+ *     [T, 4, 256], one shared w[256]: #8208 page, description.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates nothing and never synchronises the host; every launch is
+ *     asynchronous on `stream` (NULL = the legacy default stream).
+ *   - A tensor is described by cake_tensor: base pointer plus element strides
+ *     between tokens and between heads; the hidden dimension is contiguous.
+ *     Row r of a [T, nh, H] view is (t, k) = (r / nh, r % nh).
+ *   - Activations (x, residual, y, h_new, dy, dh, dx) are BF16; w is BF16 or
+ *     FP32 (w_dtype); rstd and dw are FP32.
+ *   - H must be a positive multiple of 8 and at most CAKE_MAX_HIDDEN; every
+ *     activation base pointer and w must be 16-byte aligned and every stride a
+ *     multiple of 8 elements (16 bytes), else CAKE_ERR_UNSUPPORTED.
+ *   - rows = T * nh must be below 2^31.
+ *   - Return codes come from host-side validation and from the CUDA launch
+ *     (cudaGetLastError).  Faults that happen later on the device surface at
+ *     the caller's next synchronisation, as with any CUDA call; the kernels'
+ *     own bounded waits report through cake_rmsnorm_device_status().
+ */
+#ifndef CAKE_RMSNORM_H
+#define CAKE_RMSNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CAKE_ABI_VERSION 1
+#define CAKE_MAX_HIDDEN 8192
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *cake_stream_t;
+
+typedef enum {
+    CAKE_OK = 0,
+    CAKE_ERR_INVALID = 1,     /* null pointer, negative size, bad enum */
+    CAKE_ERR_UNSUPPORTED = 2, /* H or alignment outside what the kernels take */
+    CAKE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    CAKE_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+    CAKE_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (device status) */
+} cake_status;
+
+typedef enum { CAKE_BF16 = 0, CAKE_FP32 = 1 } cake_dtype;
+
+/* Shape of the row set: T tokens, nh heads per token, H elements per row.
+ * Plain [T, H] rows are nh = 1. */
+typedef struct {
+    int64_t tokens;
+    int64_t heads;
+    int64_t hidden;
+} cake_shape;
+
+/* A BF16 activation tensor: element (t, k, j) lives at
+ * data + t*stride_token + k*stride_head + j. */
+typedef struct {
+    void *data;
+    int64_t stride_token;
+    int64_t stride_head;
+} cake_tensor;
+
+/*
+ * Forward.  x: input rows.  residual: NULL or a tensor whose data is NULL for
+ * plain rows; otherwise h = bf16(x + residual) is normalised and written to
+ * h_new (required then, NULL otherwise).  w: [H] of w_dtype.  eps: added to
+ * the mean square in FP32.  y: output rows.  rstd: [T*nh] FP32, row-major
+ * over (t, k).  T = 0 is a no-op returning CAKE_OK.
+ * The same kernels serve both backward modes, so y, rstd and h_new do not
+ * depend on any mode, and a recomputed forward is bitwise equal to the first.
+ */
+cake_status cake_rmsnorm_fwd(const cake_shape *shape, const cake_tensor *x,
+                             const cake_tensor *residual, const void *w,
+                             cake_dtype w_dtype, float eps, const cake_tensor *y,
+                             const cake_tensor *h_new, float *rstd,
+                             cake_stream_t stream);
+
+/*
+ * Bytes of workspace cake_rmsnorm_bwd needs for this shape and mode
+ * (0 only for T = 0).  The workspace holds the CTA partials of the
+ * deterministic pair and the FP64 column accumulators and arrival counter of
+ * the single kernel, in separate regions.
+ */
+size_t cake_rmsnorm_bwd_workspace_size(const cake_shape *shape, cake_dtype w_dtype,
+                                       int deterministic);
+
+/*
+ * Zero a workspace before its first use (an asynchronous memset on stream).
+ * The single kernel needs its accumulator region to start at zero and leaves
+ * it at zero again when it completes, so this is needed once per workspace
+ * (and again only after a CAKE_ERR_TIMEOUT).  Calls that share a workspace
+ * must be ordered on one stream.
+ */
+cake_status cake_rmsnorm_bwd_workspace_init(void *workspace, size_t workspace_bytes,
+                                            cake_stream_t stream);
+
+/*
+ * Backward.  dy: gradient of y.  x: the normalised input (x for plain rows,
+ * the saved h_new on the residual route).  rstd: the forward's FP32 rstd.
+ * dh: NULL, or the gradient that reaches h_new directly on the residual route
+ * (added into dx, which is then the gradient of both x and residual).
+ * dx: output rows (may not alias dy, x or dh).  dw: [H] FP32, overwritten.
+ * deterministic != 0: the main + fixed-order reduce pair; dw is bitwise
+ * reproducible for equal inputs and shape.  deterministic == 0: the window
+ * table may pick the single kernel (FP64 column accumulation in L2 atomics);
+ * dw is then not bitwise reproducible.  dx is the same bits in every mode and
+ * variant.  T = 0: dw is zero-filled and CAKE_OK returned.
+ */
+cake_status cake_rmsnorm_bwd(const cake_shape *shape, const cake_tensor *dy,
+                             const cake_tensor *x, const float *rstd, const void *w,
+                             cake_dtype w_dtype, const cake_tensor *dh,
+                             const cake_tensor *dx, float *dw, void *workspace,
+                             size_t workspace_bytes, int deterministic,
+                             cake_stream_t stream);
+
+/* ---- variant table (host only; usable without a GPU) ------------------- */
+
+/* How the per-thread dw column sums accumulate over a CTA's rows. */
+typedef enum {
+    CAKE_DW_PLAIN = 0,  /* FP32 running sum */
+    CAKE_DW_BLOCKED = 1, /* FP32 sums over blocks of rows, folded into a
+                            compensated (hi, lo) pair */
+    CAKE_DW_TWOSUM = 2  /* error-free TwoSum per element, with the product's
+                            rounding error kept as well */
+} cake_dw_accum;
+
+typedef struct {
+    int single;        /* 0: main + fixed-order reduce pair; 1: single kernel */
+    int dw_accum;      /* cake_dw_accum */
+    int vec_per_thread; /* 16-byte vectors of a row held by each thread */
+    int warps_per_row; /* warps that share one row */
+    int row_groups;    /* rows in flight per CTA (one per group of warps_per_row warps) */
+    int stages;        /* depth of the shared-memory ring */
+    int ctas;          /* CTAs launched (P, also the number of dw partials) */
+    int64_t rows_per_cta; /* contiguous rows each CTA owns */
+    size_t smem_bytes; /* dynamic shared memory per CTA */
+} cake_variant;
+
+/*
+ * Fill *out with the variant the window table picks for this shape, weight
+ * dtype, mode and residual gradient.  force_single / force_accum (-1 = let
+ * the table decide) override the table, as the tests that sweep every variant
+ * do; deterministic = 1 refuses force_single = 1 with CAKE_ERR_INVALID.
+ */
+cake_status cake_rmsnorm_bwd_select(const cake_shape *shape, cake_dtype w_dtype,
+                                    int deterministic, int has_dh, int force_single,
+                                    int force_accum, cake_variant *out);
+
+/* cake_rmsnorm_bwd with the variant forced as in cake_rmsnorm_bwd_select. */
+cake_status cake_rmsnorm_bwd_forced(const cake_shape *shape, const cake_tensor *dy,
+                                    const cake_tensor *x, const float *rstd,
+                                    const void *w, cake_dtype w_dtype,
+                                    const cake_tensor *dh, const cake_tensor *dx,
+                                    float *dw, void *workspace, size_t workspace_bytes,
+                                    int deterministic, int force_single,
+                                    int force_accum, cake_stream_t stream);
+
+/* ---- status ------------------------------------------------------------ */
+
+/* Static text for a status code. */
+const char *cake_status_str(cake_status status);
+
+/*
+ * Read the device status word that kernels set when a bounded wait runs out
+ * (CAKE_OK or CAKE_ERR_TIMEOUT) on the current device; clear != 0 resets it.
+ * Synchronises the device.  Returns CAKE_ERR_CUDA if the read itself fails.
+ */
+cake_status cake_rmsnorm_device_status(int *code, int clear);
+
+/* CAKE_ABI_VERSION of the loaded library. */
+int cake_rmsnorm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAKE_RMSNORM_H */

@@ -166,20 +166,22 @@ def _weight(w):
     return w, 0
 
 
-def fwd_rows(T, nh, H, x: View, w, eps, residual: View | None = None, rstd_in=None, rows=None):
+def fwd_rows(T, nh, H, x: View, w, eps, residual: View | None = None, rstd_in=None, rows=None,
+             want_y: bool = True, want_h: bool = True):
     """Forward over the listed rows (None: all).
 
-    Returns (y FP64 [n, H], rstd64 [n], h_new BF16 bits [n, H]).  y uses
-    ``rstd_in`` (the kernel's FP32 rstd, indexed by row) when given.
+    Returns (y FP64 [n, H], rstd64 [n], h_new BF16 bits [n, H]); y or h_new is
+    None when not wanted.  y uses ``rstd_in`` (an FP32 rstd, indexed by row)
+    when given, else rstd64.
     """
     rows, n = _rows_arg(rows)
     if rows is None:
         n = T * nh
     w, wf = _weight(w)
     rin = None if rstd_in is None else np.ascontiguousarray(rstd_in, dtype=np.float32)
-    y = np.empty((n, H))
+    y = np.empty((n, H)) if want_y else None
     r64 = np.empty(n)
-    hn = np.empty((n, H), dtype=np.uint16)
+    hn = np.empty((n, H), dtype=np.uint16) if want_h else None
     work = np.empty(3 * H)
     res_base = residual.base() if residual is not None else None
     _check(_load().cake_oracle_fwd_rows(

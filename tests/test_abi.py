@@ -1,0 +1,189 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function the header declares, and its host-side logic (argument validation,
+the window table, workspace sizing) behaves as documented.  No call here
+launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cake_rmsnorm.h")
+
+
+@pytest.fixture(scope="module")
+def cake():
+    from bwd_dw_column_gb300 import _build
+    _build.build()
+    import bwd_dw_column_gb300 as cake
+    cake.load_library()
+    return cake
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cake_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("cake_rmsnorm_fwd", "cake_rmsnorm_bwd", "cake_rmsnorm_bwd_workspace_size"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(cake):
+    lib = cake.load_library()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", cake.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (cake_[a-z0-9_]+)\b", out))
+    assert set(_declared_functions()) <= exported
+
+
+def test_abi_version_and_status_strings(cake):
+    lib = cake.load_library()
+    assert lib.cake_rmsnorm_abi_version() == 1
+    for code in range(6):
+        assert cake.cake_status_str(code)
+    assert cake.cake_status_str(99) == "unknown status"
+
+
+def test_library_is_sm103a_only(cake):
+    out = subprocess.run(["cuobjdump", "--list-elf", cake.LIB_PATH], capture_output=True, text=True).stdout
+    archs = set(re.findall(r"sm_(\d+a?)", out))
+    assert archs == {"103a"}, archs
+
+
+# ------------------------------------------------------------ window table
+
+@pytest.mark.parametrize("H", [8, 16, 256, 512, 1536, 2048, 4096, 5120, 6144, 8192])
+@pytest.mark.parametrize("T", [1, 37, 256, 65536, 131072])
+def test_select_is_a_valid_launch(cake, H, T):
+    for det in (True, False):
+        v = cake.cake_rmsnorm_bwd_select((T, 1, H), deterministic=det)
+        threads = 32 * (v["row_groups"] * v["warps_per_row"] + 1)
+        assert threads <= (576 if v["vec_per_thread"] == 1 else 512)
+        assert v["smem_bytes"] <= 227 * 1024
+        assert 2 <= v["stages"] <= 16
+        assert v["vec_per_thread"] * 32 * v["warps_per_row"] * 8 >= H
+        assert v["ctas"] * v["rows_per_cta"] >= T and (v["ctas"] - 1) * v["rows_per_cta"] < T
+        assert v["ctas"] <= 152 * 4
+        assert v["single"] == (0 if det else 1)
+
+
+def test_row_layout_depends_on_h_alone(cake):
+    for H in (256, 1536, 2048, 6144):
+        layouts = set()
+        for T in (1, 5, 300, 70000):
+            for det in (True, False):
+                for dh in (False, True):
+                    v = cake.cake_rmsnorm_bwd_select((T, 1, H), deterministic=det, has_dh=dh)
+                    layouts.add((v["vec_per_thread"], v["warps_per_row"]))
+        assert len(layouts) == 1, (H, layouts)
+
+
+def test_partition_depends_on_shape_alone(cake):
+    a = cake.cake_rmsnorm_bwd_select((65536, 1, 2048), deterministic=True)
+    b = cake.cake_rmsnorm_bwd_select((65536, 1, 2048), deterministic=True)
+    assert a == b
+    heads = cake.cake_rmsnorm_bwd_select((32768, 24, 256), deterministic=True)
+    assert heads["ctas"] * heads["rows_per_cta"] >= 32768 * 24
+
+
+def test_forced_variants(cake):
+    for accum in (cake.DW_PLAIN, cake.DW_BLOCKED, cake.DW_TWOSUM):
+        v = cake.cake_rmsnorm_bwd_select((1000, 1, 2048), deterministic=False, force_single=1, force_accum=accum)
+        assert v["single"] == 1 and v["dw_accum"] == accum
+        v = cake.cake_rmsnorm_bwd_select((1000, 1, 2048), deterministic=True, force_single=0, force_accum=accum)
+        assert v["single"] == 0 and v["dw_accum"] == accum
+    with pytest.raises(cake.CakeError) as e:
+        cake.cake_rmsnorm_bwd_select((1000, 1, 2048), deterministic=True, force_single=1)
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("shape,status", [
+    ((10, 1, 12), 2),          # H not a multiple of 8
+    ((10, 1, 8200), 2),        # H above the maximum
+    ((-1, 1, 256), 1),         # negative T
+    ((10, 0, 256), 1),         # no heads
+    ((1 << 30, 4, 256), 2),    # 2^32 rows
+])
+def test_select_rejects_bad_shapes(cake, shape, status):
+    with pytest.raises(cake.CakeError) as e:
+        cake.cake_rmsnorm_bwd_select(shape)
+    assert e.value.status == status
+
+
+def test_workspace_size(cake):
+    assert cake.cake_rmsnorm_bwd_workspace_size((0, 1, 2048)) == 0
+    n = cake.cake_rmsnorm_bwd_workspace_size((65536, 1, 2048))
+    v = cake.cake_rmsnorm_bwd_select((65536, 1, 2048))
+    assert n >= v["ctas"] * 2048 * 8 + 2048 * 8
+    assert n < 64 << 20
+    big = cake.cake_rmsnorm_bwd_workspace_size((131072, 1, 6144), deterministic=False)
+    assert big >= 6144 * 8
+
+
+# ------------------------------------------------------ argument validation
+# Fake, never-dereferenced device addresses: validation rejects the call
+# before any CUDA runtime call is made.
+
+def _T(addr, st, sh=0):
+    from bwd_dw_column_gb300 import _Tensor
+    return _Tensor(addr, st, sh)
+
+
+def _S(T, nh, H):
+    from bwd_dw_column_gb300 import _Shape
+    return _Shape(T, nh, H)
+
+
+def _fwd(cake, shape, x, res, w, y, hn, rstd, eps=1e-6, wd=0):
+    lib = cake.load_library()
+    r = lambda t: ctypes.byref(t) if t is not None else None
+    return lib.cake_rmsnorm_fwd(r(shape), r(x), r(res), w, wd, eps, r(y), r(hn), rstd, None)
+
+
+def test_fwd_validation(cake):
+    A = 0x100000
+    ok_shape = _S(4, 1, 64)
+    good = lambda: _T(A, 64)
+    assert _fwd(cake, ok_shape, good(), None, A, good(), None, A + 4096) != 1  # would launch (no GPU here)
+    assert _fwd(cake, None, good(), None, A, good(), None, A) == 1
+    assert _fwd(cake, ok_shape, None, None, A, good(), None, A) == 1
+    assert _fwd(cake, ok_shape, _T(A + 2, 64), None, A, good(), None, A) == 2      # misaligned x
+    assert _fwd(cake, ok_shape, _T(A, 60), None, A, good(), None, A) == 2          # stride not 16 B
+    assert _fwd(cake, ok_shape, good(), None, A + 8, good(), None, A) == 2         # misaligned w
+    assert _fwd(cake, ok_shape, good(), None, A, good(), None, A + 2) == 2         # misaligned rstd
+    assert _fwd(cake, ok_shape, good(), good(), A, good(), None, A) == 1           # residual without h_new
+    assert _fwd(cake, ok_shape, good(), None, A, good(), good(), A) == 1           # h_new without residual
+    assert _fwd(cake, ok_shape, good(), None, A, good(), None, A, eps=float("nan")) == 1
+    assert _fwd(cake, ok_shape, good(), None, A, good(), None, A, wd=7) == 1
+    assert _fwd(cake, _S(0, 1, 64), None, None, None, None, None, None) == 0      # T = 0: no-op
+
+
+def _bwd(cake, shape, dy, x, rstd, w, dh, dx, dw, ws, nbytes, det=1, wd=0):
+    lib = cake.load_library()
+    r = lambda t: ctypes.byref(t) if t is not None else None
+    return lib.cake_rmsnorm_bwd(r(shape), r(dy), r(x), rstd, w, wd, r(dh), r(dx), dw, ws, nbytes, det, None)
+
+
+def test_bwd_validation(cake):
+    A = 0x100000
+    shape = _S(300, 1, 2048)
+    need = cake.cake_rmsnorm_bwd_workspace_size((300, 1, 2048))
+    t = lambda: _T(A, 2048)
+    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A, need - 1) == 3      # workspace too small
+    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, None, need) == 3       # no workspace
+    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A + 16, need) == 2     # workspace not 256-B aligned
+    assert _bwd(cake, shape, t(), t(), None, A, None, t(), A, A, need) == 1       # no rstd
+    assert _bwd(cake, shape, t(), t(), A, A, None, t(), None, A, need) == 1       # no dw
+    assert _bwd(cake, shape, _T(A, 2040), t(), A, A, None, t(), A, A, need) == 2  # rows overlap
+    assert _bwd(cake, _S(300, 1, 2044), t(), t(), A, A, None, t(), A, A, need) == 2
+    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A, need, wd=3) == 1
+    heads = _S(16, 24, 256)
+    assert _bwd(cake, heads, _T(A, 24 * 256, 256), _T(A, 24 * 512, 100), A, A, None,
+                _T(A, 24 * 256, 256), A, A, 1 << 24) == 2                           # head stride not 16 B

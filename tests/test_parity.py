@@ -1,0 +1,282 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle,
+element by element, on seeded synthetic inputs.
+
+Bars (the benchmark spec's tolerances, restated in tests/tolerances.py):
+  y     within one BF16 step of RNE_bf16(y64);
+  rstd  relative error <= 1e-6 against rstd64;
+  h_new bitwise equal to the oracle's RNE_bf16(x + residual);
+  dx    within one BF16 step of RNE_bf16(dx64) at the rstd the backward was
+        given (with the documented FP32-evaluation allowance near
+        cancellation; strict counts are reported as well);
+  dw    per element |dw - dw64| <= 1e-4 + 1e-4 |dw64| (worst element
+        reported as a fraction of that budget);
+  determinism: dx bitwise identical across calls, modes and variants; dw
+        bitwise identical across calls in deterministic mode.
+
+The backward's rstd input is the oracle's rstd64 rounded to FP32 and, on the
+residual route, its x input is the oracle's h_new: no oracle input ever comes
+from the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cake_inputs
+import oracle
+from tests import tolerances as tol
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module")
+def cake():
+    import __graft_entry__
+    __graft_entry__.build()
+    import bwd_dw_column_gb300 as cake
+    yield cake
+    assert cake.cake_rmsnorm_device_status() == 0
+
+
+def to_dev(t: torch.Tensor | None) -> torch.Tensor | None:
+    """Copy to the GPU keeping a strided view strided (copy its whole storage)."""
+    if t is None:
+        return None
+    if t.is_contiguous():
+        return t.to(DEV)
+    flat = t.as_strided((t.untyped_storage().nbytes() // t.element_size(),), (1,), 0)
+    return flat.to(DEV).as_strided(t.shape, t.stride(), t.storage_offset())
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def view_of(t: torch.Tensor) -> oracle.View:
+    """Oracle view of a (possibly strided) CPU BF16 tensor [T, H] or [T, nh, H]."""
+    base = t
+    if t.dim() == 3 and not t.is_contiguous():
+        base = t.as_strided((t.untyped_storage().nbytes() // 2,), (1,), 0)
+        flat = base.contiguous().view(torch.int16).numpy().view(np.uint16)
+        return oracle.View(flat, t.stride(0), t.stride(1), t.storage_offset())
+    b = bits(t)
+    return oracle.View.contiguous(b)
+
+
+def wbits(w: torch.Tensor):
+    return w.numpy() if w.dtype == torch.float32 else bits(w)
+
+
+def w64(w: torch.Tensor):
+    return w.double().numpy()
+
+
+def rows_f64(t: torch.Tensor) -> np.ndarray:
+    T = t.shape[0]
+    H = t.shape[-1]
+    return t.reshape(-1, H).double().numpy() if t.is_contiguous() else t.contiguous().reshape(-1, H).double().numpy()
+
+
+# --------------------------------------------------------------------- fwd
+
+def check_fwd(cake, x, w, eps, residual=None):
+    T = x.shape[0]
+    nh = x.shape[1] if x.dim() == 3 else 1
+    H = x.shape[-1]
+    y64, r64, hn = oracle.fwd_rows(T, nh, H, view_of(x), wbits(w), eps,
+                                   residual=view_of(residual) if residual is not None else None)
+    x_d = to_dev(x)
+    assert x_d.stride() == x.stride()
+    out = cake.cake_rmsnorm_fwd(x_d, w.to(DEV), eps, residual=to_dev(residual))
+    torch.cuda.synchronize()
+    y, rstd = out[0], out[1]
+    yb = bits(y).reshape(-1, H)
+    assert tol.ulp_distance(yb, oracle.bf16_round(y64)).max(initial=0) <= 1
+    rk = rstd.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(rk / r64 - 1) <= tol.RSTD_REL)
+    if residual is not None:
+        np.testing.assert_array_equal(bits(out[2]).reshape(-1, H), hn)
+    # a recomputed forward is the same bits (checkpointed recompute)
+    out2 = cake.cake_rmsnorm_fwd(x_d, w.to(DEV), eps, residual=to_dev(residual))
+    torch.cuda.synchronize()
+    assert torch.equal(out2[0], y) and torch.equal(out2[1], rstd)
+    return r64, hn
+
+
+FWD_SHAPES = [(1, 8), (3, 24), (37, 256), (5, 520), (300, 1536), (129, 2048), (33, 4096), (17, 5120), (40, 6144),
+              (9, 8192)]
+
+
+@pytest.mark.parametrize("T,H", FWD_SHAPES)
+@pytest.mark.parametrize("w_dtype", [torch.bfloat16, torch.float32])
+def test_fwd_plain(cake, T, H, w_dtype):
+    c = cake_inputs.plain_case(T, H, w_dtype=w_dtype, seed=T + H)
+    check_fwd(cake, c["x"], c["w"], c["eps"])
+
+
+@pytest.mark.parametrize("T,H", [(1, 8), (37, 256), (300, 1536), (65, 6144)])
+def test_fwd_residual(cake, T, H):
+    c = cake_inputs.residual_case(T, H, seed=H)
+    check_fwd(cake, c["x"], c["w"], c["eps"], residual=c["residual"])
+
+
+def test_fwd_outlier_and_offset_families(cake):
+    for fam in ("outlier", "offset"):
+        c = cake_inputs.plain_case(500, 2048, family=fam, w_dtype=torch.float32, seed=3)
+        check_fwd(cake, c["x"], c["w"], c["eps"])
+
+
+@pytest.mark.parametrize("T,heads,strided", [(1, 24, True), (7, 24, True), (300, 24, True), (5, 4, False),
+                                             (300, 4, False)])
+def test_fwd_per_head(cake, T, heads, strided):
+    c = cake_inputs.heads_case(T, heads, strided=strided, seed=T)
+    check_fwd(cake, c["x"], c["w"], c["eps"])
+
+
+def test_fwd_empty(cake):
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
+    w = torch.ones(256, dtype=torch.bfloat16, device=DEV)
+    y, rstd = cake.cake_rmsnorm_fwd(x, w)
+    assert y.shape == (0, 256) and rstd.numel() == 0
+
+
+# --------------------------------------------------------------------- bwd
+
+VARIANTS = [(0, tol_acc) for tol_acc in (0, 1, 2)] + [(1, tol_acc) for tol_acc in (0, 1, 2)]
+
+
+def oracle_bwd_inputs(x, w, eps, residual=None):
+    """rstd (FP32 of the oracle's rstd64) and the normalised input h (bits)."""
+    T = x.shape[0]
+    nh = x.shape[1] if x.dim() == 3 else 1
+    H = x.shape[-1]
+    _, r64, hn = oracle.fwd_rows(T, nh, H, view_of(x), wbits(w), eps,
+                                 residual=view_of(residual) if residual is not None else None, want_y=False,
+                                 want_h=residual is not None)
+    return r64.astype(np.float32), hn
+
+
+def check_bwd(cake, x, dy, w, eps, residual=None, dh=None, variants=VARIANTS, dw_gate=1.0):
+    """Run every listed (single, accum) variant; return the worst dw fraction."""
+    T = x.shape[0]
+    nh = x.shape[1] if x.dim() == 3 else 1
+    H = x.shape[-1]
+    rin, hn = oracle_bwd_inputs(x, w, eps, residual)
+    if residual is not None:
+        h_cpu = torch.from_numpy(hn.view(np.int16)).view(torch.bfloat16).reshape(x.shape)
+    else:
+        h_cpu = x
+    hv, dyv = view_of(h_cpu), view_of(dy)
+    dhv = view_of(dh) if dh is not None else None
+    dx64 = oracle.bwd_rows(T, nh, H, dyv, hv, rin, wbits(w), dh=dhv)
+    dw64 = oracle.dw_cols(T, nh, H, dyv, hv, rin)
+    dyf, hf = rows_f64(dy), rows_f64(h_cpu)
+    dhf = rows_f64(dh) if dh is not None else None
+    h_d, dy_d, w_d = to_dev(h_cpu), to_dev(dy), w.to(DEV)
+    assert h_d.stride() == h_cpu.stride()
+    r_d = torch.from_numpy(rin).to(DEV)
+    dh_d = to_dev(dh)
+    ws = cake.cake_rmsnorm_bwd_workspace(h_d, w.dtype, deterministic=False)
+    dx_ref_bits = None
+    worst = 0.0
+    for single, acc in variants:
+        det = not single
+        outs = []
+        for rep in range(2):
+            dx, dw = cake.cake_rmsnorm_bwd_forced(dy_d, h_d, r_d, w_d, dh_d, deterministic=det, force_single=single,
+                                                  force_accum=acc, workspace=ws)
+            torch.cuda.synchronize()
+            outs.append((bits(dx).reshape(-1, H), dw.cpu().numpy()))
+        (dxb, dwk), (dxb2, dwk2) = outs
+        np.testing.assert_array_equal(dxb, dxb2)
+        if det:
+            np.testing.assert_array_equal(dwk, dwk2)
+        if dx_ref_bits is None:
+            strict, bounded = tol.dx_check(dxb, dx64, dyf, hf, w64(w), rin, oracle.bf16_round, oracle.bf16_bits_to_f64,
+                                           dh=dhf)
+            assert bounded == 0, f"dx: {strict} strict / {bounded} bounded violations"
+            dx_ref_bits = dxb
+        else:
+            np.testing.assert_array_equal(dxb, dx_ref_bits)  # dx: same bits in every variant
+        for dwv in (dwk, dwk2):
+            frac = tol.dw_budget_fraction(dwv, dw64).max(initial=0.0)
+            worst = max(worst, float(frac))
+            assert frac <= dw_gate, f"dw worst {frac:.4f} of budget (single={single}, accum={acc})"
+    # the default entry point in both modes gives the same dx bits
+    for det in (True, False):
+        dx, dw = cake.cake_rmsnorm_bwd(dy_d, h_d, r_d, w_d, dh_d, deterministic=det, workspace=ws)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits(dx).reshape(-1, H), dx_ref_bits)
+        assert tol.dw_budget_fraction(dw.cpu().numpy(), dw64).max(initial=0.0) <= dw_gate
+    return worst
+
+
+BWD_SHAPES = [(1, 8), (2, 16), (3, 24), (37, 256), (5, 520), (300, 1536), (129, 2048), (33, 4096), (17, 5120),
+              (40, 6144), (9, 8192), (1000, 2048)]
+
+
+@pytest.mark.parametrize("T,H", BWD_SHAPES)
+@pytest.mark.parametrize("w_dtype", [torch.bfloat16, torch.float32])
+def test_bwd_plain(cake, T, H, w_dtype):
+    c = cake_inputs.plain_case(T, H, w_dtype=w_dtype, seed=7 * T + H)
+    check_bwd(cake, c["x"], c["dy"], c["w"], c["eps"])
+
+
+@pytest.mark.parametrize("T,H", [(3, 256), (300, 1536), (77, 6144)])
+def test_bwd_residual(cake, T, H):
+    c = cake_inputs.residual_case(T, H, seed=H + 1)
+    check_bwd(cake, c["x"], c["dy"], c["w"], c["eps"], residual=c["residual"], dh=c["dh"])
+    check_bwd(cake, c["x"], c["dy"], c["w"], c["eps"], residual=c["residual"], dh=None,
+              variants=[(0, 2), (1, 2)])
+
+
+@pytest.mark.parametrize("T,heads,strided", [(1, 24, True), (7, 24, True), (300, 24, True), (5, 4, False),
+                                             (300, 4, False)])
+def test_bwd_per_head(cake, T, heads, strided):
+    c = cake_inputs.heads_case(T, heads, strided=strided, seed=T + heads)
+    check_bwd(cake, c["x"], c["dy"], c["w"], c["eps"])
+
+
+def test_per_head_equals_gathered_rows(cake):
+    # the strided [T, 24, 256] view gives the same dx bits and (deterministic)
+    # the same dw bits as its gathered contiguous copy ... when the partition
+    # is the same, i.e. the same row count: compare [T, 24, 256] with
+    # [T*24, 1, 256] (both 24*T rows of 256).
+    c = cake_inputs.heads_case(64, 24, strided=True, seed=5)
+    x, dy, w = c["x"], c["dy"], c["w"]
+    rin, _ = oracle_bwd_inputs(x, w, c["eps"])
+    r_d = torch.from_numpy(rin).to(DEV)
+    dx1, dw1 = cake.cake_rmsnorm_bwd(dy.to(DEV), to_dev(x), r_d, w.to(DEV), deterministic=True)
+    xg = x.contiguous().reshape(64 * 24, 256)
+    dx2, dw2 = cake.cake_rmsnorm_bwd(dy.reshape(64 * 24, 256).to(DEV), xg.to(DEV), r_d, w.to(DEV), deterministic=True)
+    torch.cuda.synchronize()
+    assert torch.equal(dx1.reshape(-1, 256), dx2)
+    assert torch.equal(dw1, dw2)
+
+
+def test_bwd_empty(cake):
+    x = torch.empty((0, 2048), dtype=torch.bfloat16, device=DEV)
+    w = torch.ones(2048, dtype=torch.float32, device=DEV)
+    dw = torch.full((2048,), 7.0, device=DEV)
+    cake.cake_rmsnorm_bwd(x, x, torch.empty(0, device=DEV), w, dw=dw, workspace=torch.zeros(256, dtype=torch.uint8,
+                                                                                               device=DEV))
+    torch.cuda.synchronize()
+    assert not dw.any()
+
+
+def test_single_kernel_leaves_workspace_clean(cake):
+    c = cake_inputs.plain_case(700, 2048, seed=11)
+    rin, _ = oracle_bwd_inputs(c["x"], c["w"], c["eps"])
+    x, dy, w, r = c["x"].to(DEV), c["dy"].to(DEV), c["w"].to(DEV), torch.from_numpy(rin).to(DEV)
+    ws = cake.cake_rmsnorm_bwd_workspace(x, w.dtype, deterministic=False)
+    first = None
+    for _ in range(5):
+        _, dw = cake.cake_rmsnorm_bwd(dy, x, r, w, deterministic=False, workspace=ws)
+        torch.cuda.synchronize()
+        if first is None:
+            first = dw.clone()
+        # FP64 accumulation: repeated calls agree to FP32 rounding of the same sum
+        assert torch.allclose(dw, first, rtol=1e-6, atol=1e-6)
+    head = ws[: 256 + 2048 * 8].cpu()
+    assert not head.any()

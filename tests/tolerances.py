@@ -24,3 +24,58 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
 
 def dw_budget_fraction(dw_k: np.ndarray, dw64: np.ndarray) -> np.ndarray:
     return np.abs(dw_k.astype(np.float64) - dw64) / (DW_ATOL + DW_RTOL * np.abs(dw64))
+
+
+def _ordered(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns mapped to integers that are consecutive along the reals."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """Number of BF16 steps between two BF16 values (0: equal, 1: neighbours)."""
+    return np.abs(_ordered(a_bits) - _ordered(b_bits))
+
+
+U32 = 2.0 ** -24
+
+
+def dx_allowance(dy: np.ndarray, h: np.ndarray, w: np.ndarray, rstd: np.ndarray) -> np.ndarray:
+    """FP32 evaluation bound of rs*(g - xhat*c) for every element of [R, H] rows.
+
+    g = dy*w and xhat = h*rs are rounded once each; c is a sum of H products
+    whose rounding error is at most 64*u*sum|g*xhat|/H (an FMA chain of 8 per
+    vector, the vectors of a thread, a 5-level butterfly and at most 24 warp
+    partials); the difference and the final product add 2u each.
+    """
+    rs = rstd.astype(np.float64)[:, None]
+    g = dy * w[None, :]
+    xh = h * rs
+    H = h.shape[1]
+    c = (g * xh).sum(axis=1, keepdims=True) / H
+    dc = 64 * U32 * np.abs(g * xh).sum(axis=1, keepdims=True) / H
+    t = g - xh * c
+    return rs * (2 * U32 * (np.abs(g) + np.abs(xh * c) + np.abs(t)) + np.abs(xh) * dc)
+
+
+def dx_check(dx_bits: np.ndarray, dx64: np.ndarray, dy: np.ndarray, h: np.ndarray, w: np.ndarray,
+             rstd: np.ndarray, bf16_round, bf16_to_f64, dh: np.ndarray | None = None):
+    """(strict, bounded) violation counts of the kernel's BF16 dx against FP64.
+
+    strict: more than one BF16 step from RNE_bf16(dx64).
+    bounded: additionally farther from dx64 than one BF16 ulp plus the FP32
+    evaluation bound of the expression (cancellation can make the exact
+    BF16 rounding of a tiny dx unreachable from FP32 arithmetic).
+    """
+    ref = bf16_round(dx64)
+    dist = ulp_distance(dx_bits, ref)
+    strict = dist > 1
+    if not strict.any():
+        return 0, 0
+    err = np.abs(bf16_to_f64(dx_bits) - dx64)
+    allow = bf16_ulp(dx64) + dx_allowance(dy, h, w, rstd)
+    if dh is not None:
+        allow = allow + 2 * U32 * np.abs(dx64)
+    bounded = strict & (err > allow)
+    return int(strict.sum()), int(bounded.sum())
