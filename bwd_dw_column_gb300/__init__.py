@@ -30,6 +30,7 @@ import torch
 
 __all__ = [
     "CakeError", "load_library", "cake_rmsnorm_fwd", "cake_rmsnorm_bwd", "cake_rmsnorm_bwd_forced",
+    "cake_rmsnorm_bwd_main", "cake_rmsnorm_bwd_reduce",
     "cake_rmsnorm_bwd_workspace_size", "cake_rmsnorm_bwd_workspace", "cake_rmsnorm_bwd_select",
     "cake_rmsnorm_device_status", "cake_status_str", "LIB_PATH", "DW_PLAIN", "DW_BLOCKED", "DW_TWOSUM",
 ]
@@ -95,6 +96,11 @@ def load_library(path: str = LIB_PATH):
         lib.cake_rmsnorm_bwd_forced.argtypes = [_P(_Shape), _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_int,
                                                 _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_size_t, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_int, _vp]
+        lib.cake_rmsnorm_bwd_main.restype = ctypes.c_int
+        lib.cake_rmsnorm_bwd_main.argtypes = [_P(_Shape), _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_int,
+                                              _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_size_t, ctypes.c_int, _vp]
+        lib.cake_rmsnorm_bwd_reduce.restype = ctypes.c_int
+        lib.cake_rmsnorm_bwd_reduce.argtypes = [_P(_Shape), ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]
         lib.cake_rmsnorm_bwd_select.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_select.argtypes = [_P(_Shape), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, _P(_Variant)]
@@ -225,7 +231,7 @@ def cake_rmsnorm_bwd_workspace(x_or_shape, w_dtype=torch.bfloat16, deterministic
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 
-def _bwd(dy, x, rstd, w, dh, deterministic, workspace, dx, dw, stream, force_single, force_accum):
+def _bwd(dy, x, rstd, w, dh, deterministic, workspace, dx, dw, stream, force_single, force_accum, main_only=False):
     lib = load_library()
     _need_cuda(dy, x, rstd, w, dh, workspace, dx, dw)
     _same_rows(x, dy, "dy")
@@ -250,7 +256,10 @@ def _bwd(dy, x, rstd, w, dh, deterministic, workspace, dx, dw, stream, force_sin
             ctypes.byref(_tensor(dh)) if dh is not None else None, ctypes.byref(_tensor(dx)),
             ctypes.c_void_p(dw.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
             workspace.numel() * workspace.element_size(), int(bool(deterministic))]
-    if force_single is None and force_accum is None:
+    if main_only:
+        st = lib.cake_rmsnorm_bwd_main(*args[:-1], -1 if force_accum is None else int(force_accum), _stream(stream))
+        _check(st, "cake_rmsnorm_bwd_main")
+    elif force_single is None and force_accum is None:
         st = lib.cake_rmsnorm_bwd(*args, _stream(stream))
         _check(st, "cake_rmsnorm_bwd")
     else:
@@ -278,6 +287,24 @@ def cake_rmsnorm_bwd_forced(dy, x, rstd, w, dh=None, deterministic=True, *, forc
                             force_accum=None, workspace=None, dx=None, dw=None, stream=None):
     """Backward with the variant forced (single kernel or pair; dw accumulation form)."""
     return _bwd(dy, x, rstd, w, dh, deterministic, workspace, dx, dw, stream, force_single, force_accum)
+
+
+def cake_rmsnorm_bwd_main(dy, x, rstd, w, dh=None, *, workspace, dx=None, dw=None, force_accum=None, stream=None):
+    """First half of the deterministic pair: dx, and the CTA dw partials into ``workspace``."""
+    return _bwd(dy, x, rstd, w, dh, True, workspace, dx, dw, stream, None, force_accum, main_only=True)[0]
+
+
+def cake_rmsnorm_bwd_reduce(x_or_shape, dw: torch.Tensor, workspace: torch.Tensor, has_dh: bool = False,
+                            stream=None) -> torch.Tensor:
+    """Second half of the deterministic pair: dw from the partials in ``workspace`` (fixed order)."""
+    lib = load_library()
+    shape = _shape(x_or_shape) if isinstance(x_or_shape, torch.Tensor) else _Shape(*x_or_shape)
+    _need_cuda(dw, workspace)
+    st = lib.cake_rmsnorm_bwd_reduce(ctypes.byref(shape), int(bool(has_dh)), ctypes.c_void_p(dw.data_ptr()),
+                                     ctypes.c_void_p(workspace.data_ptr()),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "cake_rmsnorm_bwd_reduce")
+    return dw
 
 
 def cake_rmsnorm_bwd_select(shape, w_dtype=torch.bfloat16, deterministic=True, has_dh=False,

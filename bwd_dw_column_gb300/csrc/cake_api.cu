@@ -31,6 +31,10 @@ cudaError_t ensure_smem_attr(const void *kernel, size_t smem)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess)
+        return e;
     for (auto &d : done)
         if (d.first.first == dev && d.first.second == kernel) {
             d.second = smem;
@@ -285,10 +289,13 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
     return CAKE_OK;
 }
 
+enum Phase { kWhole = 0, kMainOnly = 1 };
+
 cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_tensor *x,
                     const float *rstd, const void *w, cake_dtype w_dtype, const cake_tensor *dh,
                     const cake_tensor *dx, float *dw, void *workspace, size_t workspace_bytes,
-                    int deterministic, int force_single, int force_accum, cake_stream_t stream)
+                    int deterministic, int force_single, int force_accum, cake_stream_t stream,
+                    Phase phase = kWhole)
 {
     uint32_t rows = 0;
     const int has_dh = dh && dh->data;
@@ -342,7 +349,11 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.partials = reinterpret_cast<float2 *>(ws + ws_part_off(H));
     p.block_rows = 16;
     p.status = nullptr;
-    return cuda_status(launch_bwd(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s));
+    cudaError_t e = launch_bwd_rows(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s);
+    if (e != cudaSuccess || plan.single || phase == kMainOnly)
+        return cuda_status(e);
+    ReduceParams rp{p.partials, plan.ctas, H, dw};
+    return cuda_status(launch_dw_reduce(rp, s));
 }
 
 } // namespace
@@ -487,6 +498,41 @@ cake_status cake_rmsnorm_bwd_forced(const cake_shape *shape, const cake_tensor *
 {
     return run_bwd(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, workspace, workspace_bytes,
                    deterministic, force_single, force_accum, stream);
+}
+
+cake_status cake_rmsnorm_bwd_main(const cake_shape *shape, const cake_tensor *dy, const cake_tensor *x,
+                                  const float *rstd, const void *w, cake_dtype w_dtype,
+                                  const cake_tensor *dh, const cake_tensor *dx, float *dw,
+                                  void *workspace, size_t workspace_bytes, int force_accum,
+                                  cake_stream_t stream)
+{
+    return run_bwd(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, workspace, workspace_bytes, 1, 0,
+                   force_accum, stream, kMainOnly);
+}
+
+cake_status cake_rmsnorm_bwd_reduce(const cake_shape *shape, int has_dh, float *dw, void *workspace,
+                                    size_t workspace_bytes, cake_stream_t stream)
+{
+    uint32_t rows = 0;
+    Plan plan;
+    cake_status st = select_plan(shape, 1, has_dh, 0, -1, &plan, &rows);
+    if (st != CAKE_OK)
+        return st;
+    if (!dw)
+        return CAKE_ERR_INVALID;
+    if (!aligned16(dw))
+        return CAKE_ERR_UNSUPPORTED;
+    const int H = (int)shape->hidden;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0)
+        return cuda_status(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), s));
+    if (!workspace || workspace_bytes < ws_size(H, plan.ctas, 1))
+        return CAKE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return CAKE_ERR_UNSUPPORTED;
+    const float2 *parts = reinterpret_cast<const float2 *>(static_cast<uint8_t *>(workspace) + ws_part_off(H));
+    ReduceParams rp{parts, plan.ctas, H, dw};
+    return cuda_status(launch_dw_reduce(rp, s));
 }
 
 cake_status cake_rmsnorm_device_status(int *code, int clear)

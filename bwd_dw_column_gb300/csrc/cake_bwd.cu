@@ -348,8 +348,8 @@ static cudaError_t launch_vpt(const BwdParams &p, int single, int dwm, int ctas,
     return launch_rows<VPT, 2, false>(p, ctas, smem, stream);
 }
 
-cudaError_t launch_bwd(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
-                       cudaStream_t stream)
+cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
+                            cudaStream_t stream)
 {
     BwdParams q = p;
     if (q.status == nullptr) {
@@ -357,18 +357,19 @@ cudaError_t launch_bwd(const BwdParams &p, int vpt, int single, int dwm, int cta
         if (e != cudaSuccess)
             return e;
     }
-    cudaError_t e;
     switch (vpt) {
-    case 1: e = launch_vpt<1>(q, single, dwm, ctas, smem, stream); break;
-    case 2: e = launch_vpt<2>(q, single, dwm, ctas, smem, stream); break;
-    case 3: e = launch_vpt<3>(q, single, dwm, ctas, smem, stream); break;
-    case 4: e = launch_vpt<4>(q, single, dwm, ctas, smem, stream); break;
+    case 1: return launch_vpt<1>(q, single, dwm, ctas, smem, stream);
+    case 2: return launch_vpt<2>(q, single, dwm, ctas, smem, stream);
+    case 3: return launch_vpt<3>(q, single, dwm, ctas, smem, stream);
+    case 4: return launch_vpt<4>(q, single, dwm, ctas, smem, stream);
     default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess || single)
-        return e;
-    // the fixed-order reduce, launched as a programmatic dependent of the main kernel
-    ReduceParams rp{q.partials, ctas, q.L.nvec * 8, q.dw};
+}
+
+cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
+{
+    // launched as a programmatic dependent of the main kernel before it in
+    // the stream: its CTAs may start early and block in griddepcontrol.wait
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((rp.H + 31) / 32));
     cfg.blockDim = dim3(256);
@@ -379,7 +380,7 @@ cudaError_t launch_bwd(const BwdParams &p, int vpt, int single, int dwm, int cta
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, dw_reduce_kernel, rp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, dw_reduce_kernel, rp);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();

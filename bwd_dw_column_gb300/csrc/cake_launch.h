@@ -12,8 +12,12 @@ namespace cake {
 cudaError_t ensure_smem_attr(const void *kernel, size_t smem);
 
 cudaError_t launch_fwd(const FwdParams &p, int vpt, int ctas, size_t smem, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
-                       cudaStream_t stream);
+// The backward row kernel: the pair's main kernel (single = 0) or the
+// single kernel (single = 1).
+cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
+                            cudaStream_t stream);
+// The pair's fixed-order reduce of the CTA partials.
+cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream);
 
 cudaError_t fwd_status(int *code, int clear);
 cudaError_t bwd_status(int *code, int clear);

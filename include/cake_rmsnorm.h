@@ -32,7 +32,8 @@
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates nothing and never synchronises the host; every launch is
- *     asynchronous on `stream` (NULL = the legacy default stream).
+ *     asynchronous on `stream` (NULL = the legacy default stream).  A
+ *     workspace must be 256-byte aligned.
  *   - A tensor is described by cake_tensor: base pointer plus element strides
  *     between tokens and between heads; the hidden dimension is contiguous.
  *     Row r of a [T, nh, H] view is (t, k) = (r / nh, r % nh).
@@ -143,6 +144,30 @@ cake_status cake_rmsnorm_bwd(const cake_shape *shape, const cake_tensor *dy,
                              const cake_tensor *dx, float *dw, void *workspace,
                              size_t workspace_bytes, int deterministic,
                              cake_stream_t stream);
+
+/*
+ * The deterministic pair's two halves, for callers that schedule or time them
+ * separately.  cake_rmsnorm_bwd(..., deterministic = 1, ...) is exactly
+ * cake_rmsnorm_bwd_main followed by cake_rmsnorm_bwd_reduce on the same
+ * stream, shape and workspace.
+ *
+ * _main: dx, plus one dw partial per CTA written into the workspace
+ * (force_accum: -1 = the table's choice, else a cake_dw_accum).  dw is not
+ * written.
+ * _reduce: dw[j] = the partials of column j summed in a fixed order; reads
+ * the partials the preceding _main call left in `workspace`.  has_dh must
+ * match that call.
+ */
+cake_status cake_rmsnorm_bwd_main(const cake_shape *shape, const cake_tensor *dy,
+                                  const cake_tensor *x, const float *rstd, const void *w,
+                                  cake_dtype w_dtype, const cake_tensor *dh,
+                                  const cake_tensor *dx, float *dw, void *workspace,
+                                  size_t workspace_bytes, int force_accum,
+                                  cake_stream_t stream);
+
+cake_status cake_rmsnorm_bwd_reduce(const cake_shape *shape, int has_dh, float *dw,
+                                    void *workspace, size_t workspace_bytes,
+                                    cake_stream_t stream);
 
 /* ---- variant table (host only; usable without a GPU) ------------------- */
 
