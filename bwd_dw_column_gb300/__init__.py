@@ -30,7 +30,7 @@ import torch
 
 __all__ = [
     "CakeError", "load_library", "cake_rmsnorm_fwd", "cake_rmsnorm_bwd", "cake_rmsnorm_bwd_forced",
-    "cake_rmsnorm_bwd_main", "cake_rmsnorm_bwd_reduce",
+    "cake_rmsnorm_bwd_main", "cake_rmsnorm_bwd_reduce", "cake_rmsnorm_bwd_noalloc",
     "cake_rmsnorm_bwd_workspace_size", "cake_rmsnorm_bwd_workspace", "cake_rmsnorm_bwd_select",
     "cake_rmsnorm_device_status", "cake_status_str", "LIB_PATH", "DW_PLAIN", "DW_BLOCKED", "DW_TWOSUM",
 ]
@@ -101,6 +101,9 @@ def load_library(path: str = LIB_PATH):
                                               _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_size_t, ctypes.c_int, _vp]
         lib.cake_rmsnorm_bwd_reduce.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_reduce.argtypes = [_P(_Shape), ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.cake_rmsnorm_bwd_noalloc.restype = ctypes.c_int
+        lib.cake_rmsnorm_bwd_noalloc.argtypes = [_P(_Shape), _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_int,
+                                                 _P(_Tensor), _P(_Tensor), _vp, _vp]
         lib.cake_rmsnorm_bwd_select.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_select.argtypes = [_P(_Shape), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, _P(_Variant)]
@@ -305,6 +308,36 @@ def cake_rmsnorm_bwd_reduce(x_or_shape, dw: torch.Tensor, workspace: torch.Tenso
                                      workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "cake_rmsnorm_bwd_reduce")
     return dw
+
+
+def cake_rmsnorm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, rstd: torch.Tensor, w: torch.Tensor,
+                             dh: torch.Tensor | None = None, *, dx: torch.Tensor, dw: torch.Tensor, stream=None):
+    """Non-deterministic backward whose scratch is the library's own device array.
+
+    For callers that cannot allocate device memory for the library: no
+    workspace is passed and nothing is allocated here either, so dx and dw
+    must be given.  Calls share that scratch: keep them on one stream.
+    """
+    lib = load_library()
+    _need_cuda(dy, x, rstd, w, dh, dx, dw)
+    _same_rows(x, dy, "dy")
+    _same_rows(x, dx, "dx")
+    if dh is not None:
+        _same_rows(x, dh, "dh")
+    T, nh, H, _, _ = _rows_of(x)
+    if rstd.dtype != torch.float32 or rstd.numel() != T * nh or not rstd.is_contiguous():
+        raise ValueError("rstd must be a contiguous FP32 tensor of T*nh elements")
+    if dw.dtype != torch.float32 or dw.numel() != H or not dw.is_contiguous():
+        raise ValueError("dw must be a contiguous FP32 tensor of H elements")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    shape = _shape(x)
+    st = lib.cake_rmsnorm_bwd_noalloc(ctypes.byref(shape), ctypes.byref(_tensor(dy)), ctypes.byref(_tensor(x)),
+                                      ctypes.c_void_p(rstd.data_ptr()), ctypes.c_void_p(w.data_ptr()), _w_dtype(w),
+                                      ctypes.byref(_tensor(dh)) if dh is not None else None,
+                                      ctypes.byref(_tensor(dx)), ctypes.c_void_p(dw.data_ptr()), _stream(stream))
+    _check(st, "cake_rmsnorm_bwd_noalloc")
+    return dx, dw
 
 
 def cake_rmsnorm_bwd_select(shape, w_dtype=torch.bfloat16, deterministic=True, has_dh=False,

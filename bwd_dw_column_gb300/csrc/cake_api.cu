@@ -358,6 +358,74 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
 
 } // namespace
 
+// ---------------------------------------------------------------------------
+// Backward without any caller-provided scratch (cake_rmsnorm_bwd_noalloc).
+//
+// Some callers cannot hand the library device memory they allocated: code
+// running inside a framework that owns every allocation, or a host path that
+// must not call cudaMalloc (which can synchronise the device) in the middle
+// of a step.  For them the single kernel's scratch -- its CTA arrival counter
+// and its FP64 column accumulators -- lives in this library-owned array
+// instead of a workspace.  It is loaded with the library and stays resident
+// on every GPU that uses the library until the process exits.
+constexpr size_t kNoAllocScratchBytes = 256 + 8 * (size_t)CAKE_NOALLOC_MAX_HIDDEN;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+// Device address of g_noalloc_scratch for the current device.  In host code
+// the array's name is only a stand-in for the symbol, not a device pointer,
+// so the address is looked up once per device (with that device current)
+// and cached.
+cake_status noalloc_scratch(void **out)
+{
+    static std::mutex mu;
+    static void *addr[kNoAllocMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return CAKE_ERR_CUDA;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return CAKE_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return CAKE_OK;
+}
+
+} // namespace
+
+extern "C" cake_status cake_rmsnorm_bwd_noalloc(const cake_shape *shape, const cake_tensor *dy,
+                                                const cake_tensor *x, const float *rstd, const void *w,
+                                                cake_dtype w_dtype, const cake_tensor *dh,
+                                                const cake_tensor *dx, float *dw, cake_stream_t stream)
+{
+    if (!shape)
+        return CAKE_ERR_INVALID;
+    if (shape->hidden > CAKE_NOALLOC_MAX_HIDDEN)
+        return CAKE_ERR_WORKSPACE; // more columns than the built-in scratch holds
+    uint32_t rows = 0;
+    cake_status st = check_shape(shape, &rows);
+    if (st != CAKE_OK)
+        return st;
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != CAKE_OK)
+        return st;
+    // The counter and the accumulators must start at zero.  A completed call
+    // leaves them zero, but clear them anyway (an asynchronous memset, no
+    // allocation) so that an earlier call that stopped early cannot leak in.
+    const size_t used = 256 + 8 * (size_t)shape->hidden;
+    if (rows > 0 &&
+        cudaMemsetAsync(scratch, 0, used, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CAKE_ERR_CUDA;
+    return run_bwd(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, scratch, kNoAllocScratchBytes, 0, 1, -1,
+                   stream);
+}
+
 // ------------------------------------------------------------------- C ABI
 
 extern "C" {

@@ -211,6 +211,36 @@ cake_status cake_rmsnorm_bwd_forced(const cake_shape *shape, const cake_tensor *
                                     int deterministic, int force_single,
                                     int force_accum, cake_stream_t stream);
 
+/* ---- backward without caller scratch -------------------------------------
+ * No counterpart in the pages: an addition of this library.
+ *
+ * Some callers cannot allocate device memory for the library -- code inside
+ * a framework that owns every allocation, or a path that must not call
+ * cudaMalloc (it can synchronise the device) in the middle of a step.
+ * cake_rmsnorm_bwd_noalloc is the non-deterministic backward (the single
+ * kernel, dx identical to cake_rmsnorm_bwd) with its scratch -- the CTA
+ * arrival counter and the FP64 column accumulators -- in a library-owned
+ * device array of 256 + 8 * CAKE_NOALLOC_MAX_HIDDEN bytes (64.25 KiB), which
+ * every GPU that loads the library holds until the process exits.  The
+ * caller still passes every input and output (same meaning as
+ * cake_rmsnorm_bwd).  It allocates nothing and frees nothing.
+ *   - hidden > CAKE_NOALLOC_MAX_HIDDEN: CAKE_ERR_WORKSPACE (the built-in
+ *     scratch is too small); other argument errors as cake_rmsnorm_bwd.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call clears the scratch it uses (an asynchronous memset) before
+ *     its kernel.  All calls share the one array, so calls that overlap on
+ *     the GPU (different streams, or several host threads) race: order them
+ *     on one stream.
+ */
+#define CAKE_NOALLOC_MAX_HIDDEN 8192
+
+cake_status cake_rmsnorm_bwd_noalloc(const cake_shape *shape, const cake_tensor *dy,
+                                     const cake_tensor *x, const float *rstd, const void *w,
+                                     cake_dtype w_dtype, const cake_tensor *dh,
+                                     const cake_tensor *dx, float *dw, cake_stream_t stream);
+
 /* ---- status ------------------------------------------------------------ */
 
 /* Static text for a status code. */
