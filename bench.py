@@ -40,7 +40,7 @@ METRIC = "bwd µs & achieved HBM GB/s (fraction of GB300 peak) per (H,T,w dtype,
 WORKLOAD = "h2048_t65536_outlier_w32"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-ACCUM = {"plain": 0, "blocked": 1, "twosum": 2}
+ACCUM = {"plain": 0, "blocked": 1, "twosum": 2, "kahan": 3}
 
 
 def parse_args(argv=None):
@@ -55,6 +55,8 @@ def parse_args(argv=None):
                     help="run only the named loop(s) with few launches (for ncu); prints per-call times")
     ap.add_argument("--accum", choices=sorted(ACCUM), default=None,
                     help="with --profile: force the per-thread dw accumulation form")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --profile: time CUDA-graph replays of one call (no host launch cost)")
     return ap.parse_args(argv)
 
 
@@ -397,7 +399,15 @@ def run_profile(args):
     out = {}
     stream = torch.cuda.current_stream()
     for n in names:
-        ts = [t * 1e3 for t in time_loop(torch, fns[n], args.steps, args.warmup, None, stream)]
+        fn = fns[n]
+        if args.graph:
+            fn()  # first call on the device: attributes and addresses set up before capture
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                fns[n]()
+            fn = graph.replay
+        ts = [t * 1e3 for t in time_loop(torch, fn, args.steps, args.warmup, None, stream)]
         out[n] = {"us_median": round(statistics.median(ts), 2), "us_min": round(min(ts), 2)}
     assert cake.cake_rmsnorm_device_status() == 0
     print(json.dumps({"profile": args.workload, "accum": args.accum, "us_per_call": out}), flush=True)

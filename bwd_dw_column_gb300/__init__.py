@@ -32,7 +32,7 @@ __all__ = [
     "CakeError", "load_library", "cake_rmsnorm_fwd", "cake_rmsnorm_bwd", "cake_rmsnorm_bwd_forced",
     "cake_rmsnorm_bwd_main", "cake_rmsnorm_bwd_reduce", "cake_rmsnorm_bwd_noalloc",
     "cake_rmsnorm_bwd_workspace_size", "cake_rmsnorm_bwd_workspace", "cake_rmsnorm_bwd_select",
-    "cake_rmsnorm_device_status", "cake_status_str", "LIB_PATH", "DW_PLAIN", "DW_BLOCKED", "DW_TWOSUM",
+    "cake_rmsnorm_device_status", "cake_status_str", "cake_rmsnorm_plan_occupancy", "LIB_PATH", "DW_PLAIN", "DW_BLOCKED", "DW_TWOSUM", "DW_KAHAN",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,7 +40,7 @@ LIB_PATH = os.path.join(_HERE, "libcake_rmsnorm.so")
 
 CAKE_OK, CAKE_ERR_INVALID, CAKE_ERR_UNSUPPORTED, CAKE_ERR_WORKSPACE, CAKE_ERR_CUDA, CAKE_ERR_TIMEOUT = range(6)
 CAKE_BF16, CAKE_FP32 = 0, 1
-DW_PLAIN, DW_BLOCKED, DW_TWOSUM = 0, 1, 2
+DW_PLAIN, DW_BLOCKED, DW_TWOSUM, DW_KAHAN = 0, 1, 2, 3
 
 
 class CakeError(RuntimeError):
@@ -107,6 +107,9 @@ def load_library(path: str = LIB_PATH):
         lib.cake_rmsnorm_bwd_select.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_select.argtypes = [_P(_Shape), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, _P(_Variant)]
+        lib.cake_rmsnorm_plan_occupancy.restype = ctypes.c_int
+        lib.cake_rmsnorm_plan_occupancy.argtypes = [_P(_Shape), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    _P(ctypes.c_int), _P(ctypes.c_int)]
         lib.cake_rmsnorm_device_status.restype = ctypes.c_int
         lib.cake_rmsnorm_device_status.argtypes = [_P(ctypes.c_int), ctypes.c_int]
         _lib = lib
@@ -351,6 +354,17 @@ def cake_rmsnorm_bwd_select(shape, w_dtype=torch.bfloat16, deterministic=True, h
                                      -1 if force_accum is None else int(force_accum), ctypes.byref(v))
     _check(st, "cake_rmsnorm_bwd_select")
     return {f: getattr(v, f) for f, _ in _Variant._fields_}
+
+
+def cake_rmsnorm_plan_occupancy(shape, backward=True, has_extra=False, deterministic=True, force_accum=None):
+    """(planned, resident) CTAs per SM for the kernel a call would launch (needs the GPU)."""
+    lib = load_library()
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.cake_rmsnorm_plan_occupancy(ctypes.byref(_Shape(*shape)), int(bool(backward)), int(bool(has_extra)),
+                                         int(bool(deterministic)), -1 if force_accum is None else int(force_accum),
+                                         ctypes.byref(a), ctypes.byref(b))
+    _check(st, "cake_rmsnorm_plan_occupancy")
+    return a.value, b.value
 
 
 def cake_rmsnorm_device_status(clear: bool = True) -> int:

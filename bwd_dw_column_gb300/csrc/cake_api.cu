@@ -2,6 +2,7 @@
 // picks a variant per (H, rows, weight dtype, mode), workspace layout, and
 // dispatch to the kernel launchers.  Host code only.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <utility>
@@ -51,30 +52,89 @@ cudaError_t ensure_smem_attr(const void *kernel, size_t smem)
 // depend on the shape alone.
 constexpr int kSMs = 152;
 constexpr size_t kSmemPerSM = 220 * 1024; // budget for the rings of co-resident CTAs
-constexpr int kMaxThreads = 512;
 constexpr int kMaxStages = 16;
+
+enum Kind { kFwd = 0, kBwd = 1 };
+
+// Developer override of the table, for tuning sweeps: CAKE_TUNE holds
+// comma-separated key=value pairs among vpt, groups, cps, stages (backward)
+// and fvpt, fgroups, fcps, fstages (forward).  Unset, the table below rules.
+// A different row layout (vpt) changes the reduction order and therefore the
+// bits of dx / y / rstd; a different cps or groups changes the pair's
+// partition and therefore the bits of the deterministic dw.
+struct Tune {
+    int v[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages]
+};
+
+static Tune parse_tune(const char *t)
+{
+    Tune r;
+    if (!t)
+        return r;
+    static const char *keys[2][4] = {{"fvpt", "fgroups", "fcps", "fstages"}, {"vpt", "groups", "cps", "stages"}};
+    const char *p = t;
+    while (*p) {
+        const char *eq = strchr(p, '=');
+        if (!eq)
+            break;
+        const size_t klen = (size_t)(eq - p);
+        const int val = atoi(eq + 1);
+        for (int k = 0; k < 2; ++k)
+            for (int i = 0; i < 4; ++i)
+                if (strlen(keys[k][i]) == klen && strncmp(p, keys[k][i], klen) == 0)
+                    r.v[k][i] = val;
+        const char *comma = strchr(eq, ',');
+        if (!comma)
+            break;
+        p = comma + 1;
+    }
+    return r;
+}
+
+static const Tune &tune()
+{
+    static const Tune t = parse_tune(getenv("CAKE_TUNE"));
+    return t;
+}
 
 struct RowLayout {
     int vpt, W;
 };
 
-// The row layout fixes which thread owns which columns and therefore the
-// reduction order of every per-row sum: it depends on H alone, so dx, y and
-// rstd are the same bits whatever else the table picks.
-static RowLayout row_layout(int H)
+static RowLayout layout_for(int H, int vpt)
 {
+    const int nvec = H / 8;
+    return {vpt, (nvec + 32 * vpt - 1) / (32 * vpt)};
+}
+
+// The row layout fixes which thread owns which columns and therefore the
+// reduction order of every per-row sum.  It depends on H (and on whether it
+// is the forward or the backward) alone, so dx, y and rstd are the same bits
+// whatever else the table picks.
+//   backward: 8 columns per thread up to H = 6144 -- the backward keeps
+//     x, dy*w and the dw accumulators of its columns in registers, so few
+//     columns per thread leave room for many resident warps;
+//   forward: 16 columns per thread from H = 512 (fewer, longer rows per
+//     thread amortise the per-row reduction).
+static RowLayout row_layout(int H, Kind kind)
+{
+    const int forced = tune().v[kind][0];
+    if (forced >= 1 && forced <= 4) {
+        RowLayout l = layout_for(H, forced);
+        if ((l.W + 1) * 32 <= kMaxThreadsFor(forced))
+            return l;
+    }
     const int nvec = H / 8;
     if (nvec <= 32)
         return {1, 1};
-    if (nvec <= 64)
-        return {2, 1};
-    int vpt = 2;
-    int W = (nvec + 63) / 64;
-    while (W > 15) {
-        ++vpt;
-        W = (nvec + 32 * vpt - 1) / (32 * vpt);
+    if (kind == kBwd && nvec <= 32 * 24)
+        return layout_for(H, 1);
+    for (int vpt = 2; vpt <= 4; ++vpt) {
+        RowLayout l = layout_for(H, vpt);
+        if ((l.W + 1) * 32 <= kMaxThreadsFor(vpt))
+            return l;
     }
-    return {vpt, W};
+    return layout_for(H, 4);
 }
 
 struct Plan {
@@ -87,52 +147,72 @@ struct Plan {
 
 static size_t ring_smem(int ntens, int groups, int H, int stages)
 {
-    return (size_t)kMiscBytes + (size_t)stages * ntens * groups * H * 2;
+    return (size_t)kMiscBytes + weight_smem_bytes(H) + (size_t)stages * ntens * groups * H * 2;
+}
+
+// Registers per thread of each row kernel as compiled for sm_103a (ptxas
+// -v), by kind and VPT; the resident-CTA count below follows from them and
+// a GPU test checks it against the occupancy the runtime reports.
+static int kernel_regs(Kind kind, int vpt)
+{
+    static const int bwd[5] = {0, 72, 128, 128, 128};
+    static const int fwd[5] = {0, 48, 64, 80, 96};
+    return kind == kBwd ? bwd[vpt] : fwd[vpt];
+}
+
+static int resident_limit(Kind kind, int vpt, int warps_per_cta)
+{
+    const int regs = (kernel_regs(kind, vpt) + 7) & ~7;
+    const int by_regs = 65536 / (warps_per_cta * 32 * regs);
+    const int by_warps = 64 / warps_per_cta;
+    return by_regs < by_warps ? by_regs : by_warps;
 }
 
 // Per-H CTA shape: row groups (rows in flight) per CTA and CTAs per SM.
-static void cta_shape(int H, const RowLayout &rl, int &groups, int &ctas_per_sm)
+// About 8 consumer warps per CTA where the row allows it, then as many CTAs
+// per SM as the register file holds (at most 3).
+static void cta_shape(const RowLayout &rl, Kind kind, int &groups, int &ctas_per_sm)
 {
     const int W = rl.W;
-    const int max_warps = (rl.vpt == 1 ? 576 : kMaxThreads) / 32 - 1; // consumer warps
-    (void)H;
-    if (W == 1) {
-        groups = 16;
-        ctas_per_sm = 3;
-    } else if (W <= 4) {
-        groups = 2;
-        ctas_per_sm = W <= 3 ? 4 : 3;
-    } else if (W <= 8) {
-        groups = 1;
-        ctas_per_sm = 3;
-    } else {
-        groups = 1;
-        ctas_per_sm = 2;
-    }
+    const int max_warps = kMaxThreadsFor(rl.vpt) / 32 - 1; // consumer warps per CTA
+    groups = W >= 8 ? 1 : 8 / W;
+    const Tune &t = tune();
+    if (t.v[kind][1] > 0)
+        groups = t.v[kind][1];
     while (groups * W > max_warps && groups > 1)
         --groups;
+    ctas_per_sm = resident_limit(kind, rl.vpt, groups * W + 1);
+    if (ctas_per_sm > 3)
+        ctas_per_sm = 3;
+    if (ctas_per_sm < 1)
+        ctas_per_sm = 1;
+    if (t.v[kind][2] > 0)
+        ctas_per_sm = t.v[kind][2];
 }
 
-static Plan make_plan(int H, uint32_t rows, int ntens, int single, int dwm)
+static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, int dwm)
 {
     Plan p;
-    p.rl = row_layout(H);
-    cta_shape(H, p.rl, p.groups, p.ctas_per_sm);
+    p.rl = row_layout(H, kind);
+    cta_shape(p.rl, kind, p.groups, p.ctas_per_sm);
     const size_t per_cta = kSmemPerSM / p.ctas_per_sm;
     const size_t stage = (size_t)ntens * p.groups * H * 2;
-    int stages = (int)((per_cta - kMiscBytes) / stage);
+    const size_t fixed = (size_t)kMiscBytes + weight_smem_bytes(H);
+    int stages = per_cta > fixed ? (int)((per_cta - fixed) / stage) : 0;
+    if (tune().v[kind][3] >= 2 && tune().v[kind][3] < stages)
+        stages = tune().v[kind][3];
     if (stages > kMaxStages)
         stages = kMaxStages;
     if (stages < 2) { // fewer CTAs per SM so that at least two stages fit
         p.ctas_per_sm = 1;
-        stages = (int)((kSmemPerSM - kMiscBytes) / stage);
+        stages = (int)((kSmemPerSM - fixed) / stage);
         if (stages > kMaxStages)
             stages = kMaxStages;
     }
     p.stages = stages;
     p.smem = ring_smem(ntens, p.groups, H, stages);
     // the group-combine buffer reuses the ring
-    const size_t comb = (size_t)kMiscBytes + (size_t)(p.groups > 1 ? p.groups - 1 : 0) * H * 8;
+    const size_t comb = fixed + (size_t)(p.groups > 1 ? p.groups - 1 : 0) * H * 8;
     if (comb > p.smem)
         p.smem = comb;
     const uint32_t tile = (uint32_t)p.groups;
@@ -148,23 +228,36 @@ static Plan make_plan(int H, uint32_t rows, int ntens, int single, int dwm)
 }
 
 // Mode / accumulation choice.  Deterministic: the pair.  Non-deterministic:
-// the single kernel (FP64 column accumulation).  The per-thread accumulation
-// is the compensated TwoSum form; small row counts (a few rows per thread)
-// take the plain FP32 sum, whose error there is far inside the budget.
+// the single kernel (FP64 column accumulation in L2).  Per-thread
+// accumulation: up to 2048 rows the plain FP32 sum (a thread sums a handful
+// of rows, far inside the budget); above, Kahan's compensated sum of the
+// rounded products, which leaves only the products' own rounding and costs
+// about as much as the blocked form.
 static void pick_variant(uint32_t rows, int deterministic, int &single, int &dwm)
 {
     single = deterministic ? 0 : 1;
-    dwm = rows <= 2048 ? CAKE_DW_PLAIN : CAKE_DW_TWOSUM;
+    dwm = rows <= 2048 ? CAKE_DW_PLAIN : CAKE_DW_KAHAN;
+}
+
+// Partial ranges per column per warp of the fixed-order reduce: enough CTAs
+// (about 64 or more) for small H.
+static int reduce_slices(int H)
+{
+    int S = 1;
+    while (S < 8 && (H + 32 / S - 1) / (32 / S) < 64)
+        S *= 2;
+    return S;
 }
 
 // ---------------------------------------------------------- workspace layout
 
 constexpr size_t kWsHeader = 256; // arrival counter (+ padding)
+constexpr int kAccBanks = 8;      // copies of the single kernel's FP64 accumulators
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 static size_t ws_acc_off() { return kWsHeader; }
-static size_t ws_part_off(int H) { return align256(kWsHeader + (size_t)H * 8); }
+static size_t ws_part_off(int H) { return align256(kWsHeader + (size_t)kAccBanks * H * 8); }
 static size_t ws_size(int H, int ctas, int need_partials)
 {
     return ws_part_off(H) + (need_partials ? (size_t)ctas * H * 8 : 0);
@@ -275,7 +368,7 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
     cake_status st = check_shape(shape, rows);
     if (st != CAKE_OK)
         return st;
-    if (force_single > 1 || force_accum > CAKE_DW_TWOSUM)
+    if (force_single > 1 || force_accum > CAKE_DW_KAHAN)
         return CAKE_ERR_INVALID;
     if (deterministic && force_single == 1)
         return CAKE_ERR_INVALID;
@@ -285,7 +378,7 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
         single = force_single;
     if (force_accum >= 0)
         dwm = force_accum;
-    *plan = make_plan((int)shape->hidden, *rows, has_dh ? 3 : 2, single, dwm);
+    *plan = make_plan((int)shape->hidden, *rows, has_dh ? 3 : 2, kBwd, single, dwm);
     return CAKE_OK;
 }
 
@@ -322,7 +415,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
         return st;
     if (has_dh && (st = check_tensor(dh, shape)) != CAKE_OK)
         return st;
-    const size_t need = ws_size(H, plan.ctas, !plan.single);
+    const size_t need = plan.single ? kWsHeader + (size_t)H * 8 : ws_size(H, plan.ctas, 1);
     if (!workspace || workspace_bytes < need)
         return CAKE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -347,12 +440,18 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.arrivals = reinterpret_cast<unsigned int *>(ws);
     p.acc = reinterpret_cast<double *>(ws + ws_acc_off());
     p.partials = reinterpret_cast<float2 *>(ws + ws_part_off(H));
+    // the accumulator banks that fit the given workspace (the built-in
+    // scratch of the allocation-free entry point may hold fewer than 8)
+    {
+        const size_t room = workspace_bytes > kWsHeader ? (workspace_bytes - kWsHeader) / ((size_t)H * 8) : 0;
+        p.banks = room >= (size_t)kAccBanks ? kAccBanks : (int)(room > 0 ? room : 1);
+    }
     p.block_rows = 16;
     p.status = nullptr;
     cudaError_t e = launch_bwd_rows(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s);
     if (e != cudaSuccess || plan.single || phase == kMainOnly)
         return cuda_status(e);
-    ReduceParams rp{p.partials, plan.ctas, H, dw};
+    ReduceParams rp{p.partials, plan.ctas, H, dw, reduce_slices(H)};
     return cuda_status(launch_dw_reduce(rp, s));
 }
 
@@ -418,7 +517,7 @@ extern "C" cake_status cake_rmsnorm_bwd_noalloc(const cake_shape *shape, const c
     // The counter and the accumulators must start at zero.  A completed call
     // leaves them zero, but clear them anyway (an asynchronous memset, no
     // allocation) so that an earlier call that stopped early cannot leak in.
-    const size_t used = 256 + 8 * (size_t)shape->hidden;
+    const size_t used = kNoAllocScratchBytes;
     if (rows > 0 &&
         cudaMemsetAsync(scratch, 0, used, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return CAKE_ERR_CUDA;
@@ -475,7 +574,7 @@ cake_status cake_rmsnorm_fwd(const cake_shape *shape, const cake_tensor *x,
     }
     const int H = (int)shape->hidden;
     const int ntens = has_res ? 2 : 1;
-    Plan plan = make_plan(H, rows, ntens, 0, 0);
+    Plan plan = make_plan(H, rows, ntens, kFwd, 0, 0);
     FwdParams p{};
     p.L = make_layout(plan, H, rows, (uint32_t)shape->heads, ntens);
     p.x = make_view(x, shape);
@@ -513,7 +612,7 @@ size_t cake_rmsnorm_bwd_workspace_size(const cake_shape *shape, cake_dtype w_dty
     const int H = (int)shape->hidden;
     size_t need = 0;
     for (int ntens = 2; ntens <= 3; ++ntens) {
-        Plan p = make_plan(H, rows, ntens, 0, 0);
+        Plan p = make_plan(H, rows, ntens, kBwd, 0, 0);
         size_t n = ws_size(H, p.ctas, 1);
         if (n > need)
             need = n;
@@ -599,8 +698,37 @@ cake_status cake_rmsnorm_bwd_reduce(const cake_shape *shape, int has_dh, float *
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return CAKE_ERR_UNSUPPORTED;
     const float2 *parts = reinterpret_cast<const float2 *>(static_cast<uint8_t *>(workspace) + ws_part_off(H));
-    ReduceParams rp{parts, plan.ctas, H, dw};
+    ReduceParams rp{parts, plan.ctas, H, dw, reduce_slices(H)};
     return cuda_status(launch_dw_reduce(rp, s));
+}
+
+cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, int has_extra,
+                                        int deterministic, int force_accum, int *planned,
+                                        int *resident)
+{
+    if (!planned || !resident)
+        return CAKE_ERR_INVALID;
+    uint32_t rows = 0;
+    Plan plan;
+    cake_status st;
+    if (backward) {
+        st = select_plan(shape, deterministic, has_extra, -1, force_accum, &plan, &rows);
+    } else {
+        st = check_shape(shape, &rows);
+        if (st == CAKE_OK)
+            plan = make_plan((int)shape->hidden, rows, has_extra ? 2 : 1, kFwd, 0, 0);
+    }
+    if (st != CAKE_OK)
+        return st;
+    const int threads = 32 * (plan.groups * plan.rl.W + 1);
+    int n = 0;
+    cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.single, plan.dwm, threads, plan.smem, &n)
+                             : occupancy_fwd(plan.rl.vpt, threads, plan.smem, &n);
+    if (e != cudaSuccess)
+        return CAKE_ERR_CUDA;
+    *planned = plan.ctas_per_sm;
+    *resident = n;
+    return CAKE_OK;
 }
 
 cake_status cake_rmsnorm_device_status(int *code, int clear)

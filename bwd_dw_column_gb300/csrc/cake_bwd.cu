@@ -28,6 +28,8 @@
 // compensated pair ("kb", PR #8899 page, window list); TwoSum per-thread sums
 // with the product's rounding error kept (#8208 page, description; #8253
 // commit: "the twosum forms").
+#include <mutex>
+
 #include "cake_launch.h"
 #include "cake_rows.cuh"
 
@@ -35,8 +37,29 @@ namespace cake {
 
 __device__ int g_bwd_status;
 
+// Device address of the status word, looked up once per device.
+static cudaError_t status_ptr(int **out)
+{
+    static std::mutex mu;
+    static int *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        e = cudaGetSymbolAddress((void **)&addr[dev], g_bwd_status);
+        if (e != cudaSuccess)
+            return e;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
 template <int VPT, int DWM, bool SINGLE>
-__global__ void __launch_bounds__(VPT == 1 ? 576 : 512) bwd_rows_kernel(const __grid_constant__ BwdParams p)
+__global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const Layout &L = p.L;
@@ -63,20 +86,18 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) bwd_rows_kernel(const __
     const int nvec = L.nvec;
     const bool has_dh = L.ntens == 3;
 
-    float wf[VPT][8];
-    load_weight<VPT>(p.w, p.w_f32, nvec, gtid, W, wf);
+    stage_weight(s, L, p.w, p.w_f32);
 
-    // dw accumulators for this thread's columns
-    float hi[VPT][8], lo[VPT][8], blk[VPT][8];
+    // dw accumulators for this thread's columns (pairs of adjacent columns):
+    // the partial is hi + lo in every form.
+    float2 hi[VPT][4], lo[VPT][4], blk[VPT][4];
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            hi[k][e] = 0.f;
-            if (DWM != 0)
-                lo[k][e] = 0.f;
-            if (DWM == 1)
-                blk[k][e] = 0.f;
+        for (int q = 0; q < 4; ++q) {
+            hi[k][q] = make_float2(0.f, 0.f);
+            lo[k][q] = make_float2(0.f, 0.f);
+            blk[k][q] = make_float2(0.f, 0.f);
         }
     int blk_rows = 0;
 
@@ -84,115 +105,153 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) bwd_rows_kernel(const __
         const uint32_t r = c.r0 + tile * c.tile_rows + gid;
         return (tile < c.ntiles && r < c.r_end) ? __ldg(p.rstd + r) : 0.f;
     };
-    float rs_cur = rs_of_tile(0);
+    // rstd of this group's row, loaded four tiles ahead (a register ring)
+    float rs_cur = rs_of_tile(0), rs_n1 = rs_of_tile(1), rs_n2 = rs_of_tile(2), rs_n3 = rs_of_tile(3);
 
     bool abort = false;
     uint32_t slot = 0;
+    uint32_t st = 0, ph = 0; // ring slot of tile `it` and the parity of its round
     for (uint32_t it = 0; it < c.ntiles && !abort; ++it) {
-        const float rs_next = rs_of_tile(it + 1);
-        const uint32_t st = it % L.stages;
-        abort = !mbar_wait(smem_addr(&s.full[st]), (it / L.stages) & 1);
+        const float rs_n4 = rs_of_tile(it + 4);
+        abort = !mbar_wait(smem_addr(&s.full[st]), ph);
         const uint8_t *stage = s.ring + st * s.stage_bytes;
         const uint32_t r = c.r0 + it * c.tile_rows + gid;
         if (r < c.r_end) { // uniform across the group
             const float rs = rs_cur;
+            const float2 rs2 = make_float2(rs, rs);
+            const float2 nrs2 = make_float2(-rs, -rs);
             const uint4 *xs = reinterpret_cast<const uint4 *>(stage + gid * L.H * 2);
             const uint4 *dys = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + gid * L.H * 2);
             const uint4 *dhs = reinterpret_cast<const uint4 *>(stage + 2 * s.tens_bytes + gid * L.H * 2);
 
-            // pass 1: c = (1/H) sum g*xhat, fixed order: e within a vector, then k,
-            // then the group reduction
-            float dot = 0.f;
+            // One pass over the staged row: m = dy*w and the row dot
+            // sum m*h (even / odd columns in the two lanes, in the order of
+            // k and q; then lane 0 + lane 1; then the group reduction), and
+            // the dw terms dy*h*rstd (dy*h is exact in FP32).
+            // VPT == 1 keeps x and m in registers for the dx step; wider
+            // layouts re-read the staged row instead (fewer registers)
+            constexpr bool kKeep = VPT == 1;
+            float2 x2[kKeep ? VPT : 1][4], m2[kKeep ? VPT : 1][4];
+            float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * 32 * W + gtid;
+                uint4 xr = make_uint4(0, 0, 0, 0), dr = make_uint4(0, 0, 0, 0);
                 if (v < nvec) {
-                    float xf[8], df[8];
-                    unpack8(xs[v], xf);
-                    unpack8(dys[v], df);
-                    float d8 = 0.f;
+                    xr = xs[v];
+                    dr = dys[v];
+                }
+                float2 w2[4];
+                weight_pairs(s, L, v < nvec ? v : 0, w2);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d8 = fmaf(__fmul_rn(df[e], wf[k][e]), __fmul_rn(xf[e], rs), d8);
-                    dot = __fadd_rn(dot, d8);
+                for (int q = 0; q < 4; ++q) {
+                    const float2 xv = bf2(word(xr, q));
+                    const float2 d2 = bf2(word(dr, q));
+                    const float2 mv = mul2(d2, w2[q]);
+                    if (kKeep) {
+                        x2[kKeep ? k : 0][q] = xv;
+                        m2[kKeep ? k : 0][q] = mv;
+                    }
+                    dot2 = fma2(mv, xv, dot2);
+                    const float2 a2 = mul2(d2, xv);
+                    if (DWM == CAKE_DWM_PLAIN) {
+                        hi[k][q] = fma2(a2, rs2, hi[k][q]);
+                    } else if (DWM == CAKE_DWM_BLOCKED) {
+                        blk[k][q] = fma2(a2, rs2, blk[k][q]);
+                    } else if (DWM == CAKE_DWM_TWOSUM) {
+                        // npr = -RN(a*rs); pe = a*rs - RN(a*rs) exactly (FMA);
+                        // Knuth's TwoSum of hi and RN(a*rs) written with npr:
+                        // s = hi + pr, e = (hi - (s - (s - hi))) + (pr - (s - hi));
+                        // lo collects e and pe
+                        const float2 npr = mul2(a2, nrs2);
+                        const float2 pe = fma2(a2, rs2, npr);
+                        const float2 sm = sub2(hi[k][q], npr);
+                        const float2 bp = sub2(sm, hi[k][q]);
+                        const float2 ap = sub2(sm, bp);
+                        const float2 e = sub2(sub2(hi[k][q], ap), add2(npr, bp));
+                        hi[k][q] = sm;
+                        lo[k][q] = add2(lo[k][q], add2(e, pe));
+                    } else {
+                        // Kahan: lo holds the negated running compensation
+                        const float2 y = fma2(a2, rs2, lo[k][q]);
+                        const float2 t = add2(hi[k][q], y);
+                        lo[k][q] = add2(sub2(hi[k][q], t), y);
+                        hi[k][q] = t;
+                    }
                 }
             }
+            const float dot = __fadd_rn(dot2.x, dot2.y);
             const float tot = group_sum(dot, s, L, gid, wig, lane, slot++, abort);
-            const float cc = __fmul_rn(tot, L.inv_h);
+            // dx_j = rs*(g_j - xhat_j*c) = m_j*rs - h_j*kk, kk = rs^3 * tot / H
+            const float kk = __fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), __fmul_rn(tot, L.inv_h));
+            const float2 nk2 = make_float2(-kk, -kk);
 
-            // pass 2 (re-reads the staged row): dx and the dw terms
             uint16_t *dxrow = p.dx + out_off(p.dx_st, p.dx_sh, p.dx_row_stride, p.dx_uniform, r, L.nh);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * 32 * W + gtid;
                 if (v < nvec && !abort) {
-                    float xf[8], df[8], o[8];
-                    unpack8(xs[v], xf);
-                    unpack8(dys[v], df);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float g = __fmul_rn(df[e], wf[k][e]);
-                        const float xh = __fmul_rn(xf[e], rs);
-                        o[e] = __fmul_rn(fmaf(-xh, cc, g), rs);
+                    uint4 hv = make_uint4(0, 0, 0, 0);
+                    if (has_dh)
+                        hv = dhs[v];
+                    uint4 xr2 = make_uint4(0, 0, 0, 0), dr2 = make_uint4(0, 0, 0, 0);
+                    float2 w2[4];
+                    if (!kKeep) {
+                        xr2 = xs[v];
+                        dr2 = dys[v];
+                        weight_pairs(s, L, v, w2);
                     }
-                    if (has_dh) {
-                        float hf[8];
-                        unpack8(dhs[v], hf);
+                    uint32_t o[4];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            o[e] = __fadd_rn(o[e], hf[e]);
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 xv = kKeep ? x2[kKeep ? k : 0][q] : bf2(word(xr2, q));
+                        const float2 mv = kKeep ? m2[kKeep ? k : 0][q] : mul2(bf2(word(dr2, q)), w2[q]);
+                        float2 d = fma2(mv, rs2, mul2(xv, nk2));
+                        if (has_dh)
+                            d = add2(d, bf2(word(hv, q)));
+                        o[q] = pack2(d);
                     }
-                    __stcs(reinterpret_cast<uint4 *>(dxrow) + v, pack8(o));
-                    // dw terms: dy*h is exact in FP32; one rounding for *rstd
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float a = __fmul_rn(df[e], xf[e]);
-                        if (DWM == 0) {
-                            hi[k][e] = fmaf(a, rs, hi[k][e]);
-                        } else if (DWM == 1) {
-                            blk[k][e] = fmaf(a, rs, blk[k][e]);
-                        } else {
-                            const float pr = __fmul_rn(a, rs);
-                            const float pe = fmaf(a, rs, -pr);
-                            float sum, err;
-                            two_sum(hi[k][e], pr, sum, err);
-                            hi[k][e] = sum;
-                            lo[k][e] = __fadd_rn(lo[k][e], __fadd_rn(err, pe));
-                        }
-                    }
+                    __stcs(reinterpret_cast<uint4 *>(dxrow) + v, make_uint4(o[0], o[1], o[2], o[3]));
                 }
             }
-            if (DWM == 1 && ++blk_rows == p.block_rows) {
+            if (DWM == CAKE_DWM_BLOCKED && ++blk_rows == p.block_rows) {
                 blk_rows = 0;
 #pragma unroll
                 for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        comp_add(hi[k][e], lo[k][e], blk[k][e]);
-                        blk[k][e] = 0.f;
+                    for (int q = 0; q < 4; ++q) {
+                        float2 sum, err;
+                        two_sum2(hi[k][q], blk[k][q], sum, err);
+                        hi[k][q] = sum;
+                        lo[k][q] = add2(lo[k][q], err);
+                        blk[k][q] = make_float2(0.f, 0.f);
                     }
             }
         }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
-        rs_cur = rs_next;
+        if (++st == (uint32_t)L.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
+        rs_cur = rs_n1;
+        rs_n1 = rs_n2;
+        rs_n2 = rs_n3;
+        rs_n3 = rs_n4;
     }
     if (abort && lane == 0)
         set_status(p.status, kStatusTimeout);
-    if (DWM == 0) {
+    if (DWM == CAKE_DWM_BLOCKED) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                lo[k][e] = 0.f;
-    }
-    if (DWM == 1) {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                comp_add(hi[k][e], lo[k][e], blk[k][e]);
+            for (int q = 0; q < 4; ++q) {
+                float2 sum, err;
+                two_sum2(hi[k][q], blk[k][q], sum, err);
+                hi[k][q] = sum;
+                lo[k][q] = add2(lo[k][q], err);
+            }
     }
     if (!SINGLE)
         pdl_launch_dependents();
@@ -208,8 +267,10 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) bwd_rows_kernel(const __
                 const int v = k * 32 * W + gtid;
                 if (v < nvec)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        comb[(gid - 1) * ncol + v * 8 + e] = make_float2(hi[k][e], lo[k][e]);
+                    for (int q = 0; q < 4; ++q) {
+                        comb[(gid - 1) * ncol + v * 8 + 2 * q] = make_float2(hi[k][q].x, lo[k][q].x);
+                        comb[(gid - 1) * ncol + v * 8 + 2 * q + 1] = make_float2(hi[k][q].y, lo[k][q].y);
+                    }
             }
         }
         consumer_sync(L);
@@ -220,10 +281,13 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) bwd_rows_kernel(const __
                     const int v = k * 32 * W + gtid;
                     if (v < nvec)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float2 o = comb[(g - 1) * ncol + v * 8 + e];
-                            comp_add(hi[k][e], lo[k][e], o.x);
-                            lo[k][e] = __fadd_rn(lo[k][e], o.y);
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 a = comb[(g - 1) * ncol + v * 8 + 2 * q];
+                            const float2 b = comb[(g - 1) * ncol + v * 8 + 2 * q + 1];
+                            comp_add(hi[k][q].x, lo[k][q].x, a.x);
+                            lo[k][q].x = __fadd_rn(lo[k][q].x, a.y);
+                            comp_add(hi[k][q].y, lo[k][q].y, b.x);
+                            lo[k][q].y = __fadd_rn(lo[k][q].y, b.y);
                         }
                 }
             }
@@ -238,22 +302,27 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) bwd_rows_kernel(const __
                 const int v = k * 32 * W + gtid;
                 if (v < nvec)
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2)
-                        dst[v * 4 + e / 2] = make_float4(hi[k][e], lo[k][e], hi[k][e + 1], lo[k][e + 1]);
+                    for (int q = 0; q < 4; ++q)
+                        dst[v * 4 + q] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
             }
         }
         return;
     }
 
-    // ---- single kernel: FP64 column accumulation, the last CTA finalises
+    // ---- single kernel: FP64 column accumulation into one of `banks` copies
+    // of the accumulators (CTA b adds into bank b % banks, which spreads the
+    // L2 atomics); the last CTA to arrive sums the banks and finalises
     if (gid == 0) {
+        double *acc = p.acc + (size_t)(blockIdx.x % p.banks) * ncol;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * 32 * W + gtid;
             if (v < nvec)
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    atomicAdd(p.acc + v * 8 + e, (double)hi[k][e] + (double)lo[k][e]);
+                for (int q = 0; q < 4; ++q) {
+                    atomicAdd(acc + v * 8 + 2 * q, (double)hi[k][q].x + (double)lo[k][q].x);
+                    atomicAdd(acc + v * 8 + 2 * q + 1, (double)hi[k][q].y + (double)lo[k][q].y);
+                }
         }
         __threadfence();
     }
@@ -267,56 +336,71 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) bwd_rows_kernel(const __
         __threadfence();
         const int nthr = consumer_warps * 32;
         for (int j = threadIdx.x; j < ncol; j += nthr) {
-            const unsigned long long bits =
-                atomicExch(reinterpret_cast<unsigned long long *>(p.acc + j), 0ull);
-            p.dw[j] = (float)__longlong_as_double((long long)bits);
+            double sum = 0.0;
+            for (int b = 0; b < p.banks; ++b) {
+                sum += __ldcg(p.acc + (size_t)b * ncol + j);
+                p.acc[(size_t)b * ncol + j] = 0.0;
+            }
+            p.dw[j] = (float)sum;
         }
         if (threadIdx.x == 0)
             atomicExch(p.arrivals, 0u);
     }
 }
 
-// Fixed-order reduction of the pair's CTA partials: column j of dw is the
-// compensated sum of partials[p][j] over p ascending, split into 8 contiguous
-// ranges (one per warp) that are then combined in warp order.
-__global__ void __launch_bounds__(256) dw_reduce_kernel(const __grid_constant__ ReduceParams rp)
+// Fixed-order reduction of the pair's CTA partials.  A CTA owns C columns
+// (C = 32 / S) and 16 warps; lane = (slice s, column c).  The P partials of a
+// column are split into 16*S contiguous ranges in ascending order, range
+// w*S + s summed (compensated, ascending p, 8 loads in flight) by slice s of
+// warp w.  The ranges are then combined in range order: the S slices of a
+// column within each warp, then the 16 warps.  Small H gets more CTAs.
+constexpr int kReduceWarps = 16;
+
+__global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __grid_constant__ ReduceParams rp)
 {
-    __shared__ float2 part[8][32];
+    __shared__ float2 part[kReduceWarps][32];
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j = blockIdx.x * 32 + lane;
-    const int per = (rp.P + 7) / 8;
-    const int p0 = warp * per;
+    const int S = rp.slices, C = 32 / S;
+    const int sl = lane / C, col = lane - sl * C;
+    const int j = blockIdx.x * C + col;
+    const int nrange = kReduceWarps * S;
+    const int per = (rp.P + nrange - 1) / nrange;
+    const int p0 = (warp * S + sl) * per;
     const int p1 = min(rp.P, p0 + per);
     float hi = 0.f, lo = 0.f;
     if (j < rp.H) {
-        int q = p0;
-        for (; q + 4 <= p1; q += 4) {
-            float2 v[4];
+        for (int q = p0; q < p1; q += 8) {
+            float2 v[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                v[u] = __ldcg(rp.partials + (size_t)(q + u) * rp.H + j);
+            for (int u = 0; u < 8; ++u)
+                v[u] = q + u < p1 ? __ldcg(rp.partials + (size_t)(q + u) * rp.H + j) : make_float2(0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 comp_add(hi, lo, v[u].x);
-                lo += v[u].y;
+                lo = __fadd_rn(lo, v[u].y);
             }
         }
-        for (; q < p1; ++q) {
-            const float2 v = __ldcg(rp.partials + (size_t)q * rp.H + j);
-            comp_add(hi, lo, v.x);
-            lo += v.y;
+    }
+    // slices of a column, in slice order, into slice 0
+    for (int t = 1; t < S; ++t) {
+        const float h2 = __shfl_sync(0xffffffffu, hi, t * C + col);
+        const float l2 = __shfl_sync(0xffffffffu, lo, t * C + col);
+        if (sl == 0) {
+            comp_add(hi, lo, h2);
+            lo = __fadd_rn(lo, l2);
         }
     }
-    part[warp][lane] = make_float2(hi, lo);
+    if (sl == 0)
+        part[warp][col] = make_float2(hi, lo);
     __syncthreads();
-    if (warp == 0 && j < rp.H) {
-        float h = part[0][lane].x, l = part[0][lane].y;
-        for (int w = 1; w < 8; ++w) {
-            comp_add(h, l, part[w][lane].x);
-            l += part[w][lane].y;
+    if (warp == 0 && sl == 0 && j < rp.H) {
+        float h = part[0][col].x, l = part[0][col].y;
+        for (int w = 1; w < kReduceWarps; ++w) {
+            comp_add(h, l, part[w][col].x);
+            l = __fadd_rn(l, part[w][col].y);
         }
-        rp.dw[j] = h + l;
+        rp.dw[j] = __fadd_rn(h, l);
     }
 }
 
@@ -341,11 +425,13 @@ static cudaError_t launch_vpt(const BwdParams &p, int single, int dwm, int ctas,
     if (single) {
         if (dwm == 0) return launch_rows<VPT, 0, true>(p, ctas, smem, stream);
         if (dwm == 1) return launch_rows<VPT, 1, true>(p, ctas, smem, stream);
-        return launch_rows<VPT, 2, true>(p, ctas, smem, stream);
+        if (dwm == 2) return launch_rows<VPT, 2, true>(p, ctas, smem, stream);
+        return launch_rows<VPT, 3, true>(p, ctas, smem, stream);
     }
     if (dwm == 0) return launch_rows<VPT, 0, false>(p, ctas, smem, stream);
     if (dwm == 1) return launch_rows<VPT, 1, false>(p, ctas, smem, stream);
-    return launch_rows<VPT, 2, false>(p, ctas, smem, stream);
+    if (dwm == 2) return launch_rows<VPT, 2, false>(p, ctas, smem, stream);
+    return launch_rows<VPT, 3, false>(p, ctas, smem, stream);
 }
 
 cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
@@ -353,7 +439,7 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
 {
     BwdParams q = p;
     if (q.status == nullptr) {
-        cudaError_t e = cudaGetSymbolAddress((void **)&q.status, g_bwd_status);
+        cudaError_t e = status_ptr(&q.status);
         if (e != cudaSuccess)
             return e;
     }
@@ -371,8 +457,8 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
     // launched as a programmatic dependent of the main kernel before it in
     // the stream: its CTAs may start early and block in griddepcontrol.wait
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((rp.H + 31) / 32));
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3((unsigned)((rp.H + 32 / rp.slices - 1) / (32 / rp.slices)));
+    cfg.blockDim = dim3(32 * kReduceWarps);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -384,6 +470,42 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
+}
+
+template <int VPT, int DWM, bool SINGLE>
+static cudaError_t occ_rows(int threads, size_t smem, int *n)
+{
+    auto kern = bwd_rows_kernel<VPT, DWM, SINGLE>;
+    cudaError_t e = ensure_smem_attr((const void *)kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
+}
+
+template <int VPT>
+static cudaError_t occ_vpt(int single, int dwm, int threads, size_t smem, int *n)
+{
+    if (single) {
+        if (dwm == 0) return occ_rows<VPT, 0, true>(threads, smem, n);
+        if (dwm == 1) return occ_rows<VPT, 1, true>(threads, smem, n);
+        if (dwm == 2) return occ_rows<VPT, 2, true>(threads, smem, n);
+        return occ_rows<VPT, 3, true>(threads, smem, n);
+    }
+    if (dwm == 0) return occ_rows<VPT, 0, false>(threads, smem, n);
+    if (dwm == 1) return occ_rows<VPT, 1, false>(threads, smem, n);
+    if (dwm == 2) return occ_rows<VPT, 2, false>(threads, smem, n);
+    return occ_rows<VPT, 3, false>(threads, smem, n);
+}
+
+cudaError_t occupancy_bwd(int vpt, int single, int dwm, int threads, size_t smem, int *n)
+{
+    switch (vpt) {
+    case 1: return occ_vpt<1>(single, dwm, threads, smem, n);
+    case 2: return occ_vpt<2>(single, dwm, threads, smem, n);
+    case 3: return occ_vpt<3>(single, dwm, threads, smem, n);
+    case 4: return occ_vpt<4>(single, dwm, threads, smem, n);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t bwd_status(int *code, int clear)

@@ -56,15 +56,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One bounded test of a phase: a thread whose phase is not complete may be
+// suspended by the hardware until it completes or the hint (ns) runs out, so
+// waiting warps do not spin on the issue slots.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -79,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+        if ((i & 3u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
             return false;
     }
 }
@@ -218,3 +223,74 @@ __device__ __forceinline__ void set_status(int *status, int code)
 }
 
 }  // namespace cake
+
+namespace cake {
+
+// ------------------------------------------------------ packed FP32 pairs
+// sm_100-family packed FP32 arithmetic (PTX add/sub/mul/fma .rn.f32x2):
+// one instruction operates on two FP32 values held in a 64-bit register,
+// each rounded to nearest even exactly as the scalar instruction would.
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// a * b + c with one rounding per lane
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// BF16 pair (one 32-bit word: element 2i in the low half) -> FP32 pair.
+__device__ __forceinline__ float2 bf2(uint32_t u) { return make_float2(bf16lo(u), bf16hi(u)); }
+
+// FP32 pair -> BF16 pair, round to nearest even.
+__device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16(v.x, v.y); }
+
+__device__ __forceinline__ uint32_t word(const uint4 &v, int q)
+{
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+// TwoSum on pairs: (s, e) with s + e == a + b exactly, lane by lane.
+__device__ __forceinline__ void two_sum2(float2 a, float2 b, float2 &s, float2 &e)
+{
+    s = add2(a, b);
+    const float2 bp = sub2(s, a);
+    const float2 ap = sub2(s, bp);
+    e = add2(sub2(a, ap), sub2(b, bp));
+}
+
+} // namespace cake

@@ -11,6 +11,8 @@
 // same in both, so y, rstd and h_new are bitwise equal across modes); the
 // sum of squares has a reduction order fixed by the row layout, so a
 // recomputed forward (the checkpointed "2xfwd+bwd" step) is bitwise equal.
+#include <mutex>
+
 #include "cake_launch.h"
 #include "cake_rows.cuh"
 
@@ -18,8 +20,29 @@ namespace cake {
 
 __device__ int g_fwd_status;
 
+// Device address of the status word, looked up once per device.
+static cudaError_t status_ptr(int **out)
+{
+    static std::mutex mu;
+    static int *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        e = cudaGetSymbolAddress((void **)&addr[dev], g_fwd_status);
+        if (e != cudaSuccess)
+            return e;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
 template <int VPT>
-__global__ void __launch_bounds__(VPT == 1 ? 576 : 512) fwd_rows_kernel(const __grid_constant__ FwdParams p)
+__global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const __grid_constant__ FwdParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const Layout &L = p.L;
@@ -43,54 +66,52 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) fwd_rows_kernel(const __
     const int nvec = L.nvec;
     const bool has_res = L.ntens == 2;
 
-    float wf[VPT][8];
-    load_weight<VPT>(p.w, p.w_f32, nvec, gtid, W, wf);
+    stage_weight(s, L, p.w, p.w_f32);
 
     bool abort = false;
     uint32_t slot = 0;
+    uint32_t st = 0, ph = 0; // ring slot of tile `it` and the parity of its round
     for (uint32_t it = 0; it < c.ntiles && !abort; ++it) {
-        const uint32_t st = it % L.stages;
-        abort = !mbar_wait(smem_addr(&s.full[st]), (it / L.stages) & 1);
+        abort = !mbar_wait(smem_addr(&s.full[st]), ph);
         const uint8_t *stage = s.ring + st * s.stage_bytes;
         const uint32_t r = c.r0 + it * c.tile_rows + gid;
         if (r < c.r_end) { // uniform across the group
             const uint4 *xs = reinterpret_cast<const uint4 *>(stage + gid * L.H * 2);
             const uint4 *rsd = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + gid * L.H * 2);
-            // h = x, or bf16(x + residual) (the FP32 sum of two BF16 values
-            // rounds to the same BF16 value as the exact sum)
-            auto load_h = [&](int v) {
-                uint4 h = xs[v];
-                if (has_res) {
-                    float a[8], b[8], t[8];
-                    unpack8(h, a);
-                    unpack8(rsd[v], b);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        t[e] = __fadd_rn(a[e], b[e]);
-                    h = pack8(t);
-                }
-                return h;
-            };
-            // pass 1: sum of squares, fixed order: e within a vector, then k,
-            // then the group reduction
-            float ss = 0.f;
+            // h = x, or bf16(x + residual): the FP32 sum of two BF16 values
+            // rounds to the same BF16 value as their exact sum.  Sum of
+            // squares: even / odd columns in the two lanes in the order of k
+            // and q, then lane 0 + lane 1, then the group reduction.
+            float2 h2[VPT][4];
+            uint4 hraw[VPT];
+            float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * 32 * W + gtid;
+                uint4 h = make_uint4(0, 0, 0, 0);
                 if (v < nvec) {
-                    float hf[8];
-                    unpack8(load_h(v), hf);
-                    float s8 = 0.f;
+                    h = xs[v];
+                    if (has_res) {
+                        const uint4 rr = rsd[v];
+                        uint32_t o[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        s8 = fmaf(hf[e], hf[e], s8);
-                    ss = __fadd_rn(ss, s8);
+                        for (int q = 0; q < 4; ++q)
+                            o[q] = pack2(add2(bf2(word(h, q)), bf2(word(rr, q))));
+                        h = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+                hraw[k] = h;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    h2[k][q] = bf2(word(h, q));
+                    ss2 = fma2(h2[k][q], h2[k][q], ss2);
                 }
             }
+            const float ss = __fadd_rn(ss2.x, ss2.y);
             const float tot = group_sum(ss, s, L, gid, wig, lane, slot++, abort);
             const float rs = 1.0f / sqrtf(__fadd_rn(__fmul_rn(tot, L.inv_h), p.eps));
+            const float2 rs2 = make_float2(rs, rs);
 
-            // pass 2 (re-reads the staged row): y and h_new
             uint16_t *yrow = p.y + out_off(p.y_st, p.y_sh, p.y_row_stride, p.y_uniform, r, L.nh);
             uint16_t *hrow = has_res
                                  ? p.h_new + out_off(p.hn_st, p.hn_sh, p.hn_row_stride, p.hn_uniform, r, L.nh)
@@ -99,15 +120,15 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) fwd_rows_kernel(const __
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * 32 * W + gtid;
                 if (v < nvec && !abort) {
-                    const uint4 h = load_h(v);
-                    float hf[8], o[8];
-                    unpack8(h, hf);
+                    float2 w2[4];
+                    weight_pairs(s, L, v, w2);
+                    uint32_t o[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        o[e] = __fmul_rn(__fmul_rn(hf[e], rs), wf[k][e]);
-                    __stcs(reinterpret_cast<uint4 *>(yrow) + v, pack8(o));
+                    for (int q = 0; q < 4; ++q)
+                        o[q] = pack2(mul2(mul2(h2[k][q], rs2), w2[q]));
+                    __stcs(reinterpret_cast<uint4 *>(yrow) + v, make_uint4(o[0], o[1], o[2], o[3]));
                     if (has_res)
-                        __stcs(reinterpret_cast<uint4 *>(hrow) + v, h);
+                        __stcs(reinterpret_cast<uint4 *>(hrow) + v, hraw[k]);
                 }
             }
             if (gtid == 0 && !abort)
@@ -116,6 +137,10 @@ __global__ void __launch_bounds__(VPT == 1 ? 576 : 512) fwd_rows_kernel(const __
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
+        if (++st == (uint32_t)L.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
     }
     if (abort && lane == 0)
         set_status(p.status, kStatusTimeout);
@@ -137,7 +162,7 @@ cudaError_t launch_fwd(const FwdParams &p, int vpt, int ctas, size_t smem, cudaS
 {
     FwdParams q = p;
     if (q.status == nullptr) {
-        cudaError_t e = cudaGetSymbolAddress((void **)&q.status, g_fwd_status);
+        cudaError_t e = status_ptr(&q.status);
         if (e != cudaSuccess)
             return e;
     }
@@ -146,6 +171,27 @@ cudaError_t launch_fwd(const FwdParams &p, int vpt, int ctas, size_t smem, cudaS
     case 2: return launch_fwd_vpt<2>(q, ctas, smem, stream);
     case 3: return launch_fwd_vpt<3>(q, ctas, smem, stream);
     case 4: return launch_fwd_vpt<4>(q, ctas, smem, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int VPT>
+static cudaError_t occ_fwd(int threads, size_t smem, int *n)
+{
+    auto kern = fwd_rows_kernel<VPT>;
+    cudaError_t e = ensure_smem_attr((const void *)kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
+}
+
+cudaError_t occupancy_fwd(int vpt, int threads, size_t smem, int *n)
+{
+    switch (vpt) {
+    case 1: return occ_fwd<1>(threads, smem, n);
+    case 2: return occ_fwd<2>(threads, smem, n);
+    case 3: return occ_fwd<3>(threads, smem, n);
+    case 4: return occ_fwd<4>(threads, smem, n);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -11,6 +11,21 @@ namespace cake {
 // per-row reduction slots and flags; the staging ring follows.
 constexpr int kMiscBytes = 1024;
 
+// Shared memory for the FP32 copy of w, rounded up to 1 KB so that the ring
+// after it stays 1 KB aligned.
+__host__ __device__ constexpr unsigned weight_smem_bytes(int H) { return ((unsigned)H * 4u + 1023u) & ~1023u; }
+
+// Largest CTA (consumer warps + the producer warp) a row kernel with VPT
+// vectors per thread is compiled for; it caps the registers per thread at
+// 65536 / threads.
+__host__ __device__ constexpr int kMaxThreadsFor(int vpt) { return vpt == 1 ? 832 : 416; }
+
+// Per-thread dw accumulation forms (same values as cake_dw_accum).
+#define CAKE_DWM_PLAIN 0
+#define CAKE_DWM_BLOCKED 1
+#define CAKE_DWM_TWOSUM 2
+#define CAKE_DWM_KAHAN 3
+
 // A BF16 [T, nh, H] view.  Row r = (t, k) = (r / nh, r % nh) starts at
 // base + t*st + k*sh (elements).  When the rows are equally spaced
 // (nh == 1, or st == nh*sh) `uniform` is set and row r is at base + r*row_stride.
@@ -66,7 +81,8 @@ struct BwdParams {
     int dx_uniform;
     float *dw;          // [H]
     float2 *partials;   // pair: [ctas][H] (hi, lo)
-    double *acc;        // single: [H] FP64 column accumulators (zero between calls)
+    double *acc;        // single: [banks][H] FP64 column accumulators (zero between calls)
+    int banks;          // single: copies of the accumulators (1..16)
     unsigned int *arrivals; // single: CTA arrival counter (zero between calls)
     int block_rows;     // blocked accumulation: rows per FP32 block
     int *status;
@@ -76,6 +92,7 @@ struct ReduceParams {
     const float2 *partials; // [P][H]
     int P, H;
     float *dw;
+    int slices;             // 1, 2, 4 or 8: partial ranges per column per warp
 };
 
 } // namespace cake

@@ -27,8 +27,9 @@ constexpr int kConsumerBarrier = 9;
 struct Smem {
     uint64_t *full;   // [stages]
     uint64_t *empty;  // [stages]
-    float *red;       // [groups][2][W]
+    float *red;       // [groups][2][W] (groups * W <= 25: 200 bytes)
     int *flag;        // [4]
+    float *wsm;       // [H] the weight as FP32, staged once per CTA
     uint8_t *ring;    // stages * stage_bytes
     uint32_t stage_bytes;
     uint32_t tens_bytes; // bytes of one tensor in one stage
@@ -39,9 +40,10 @@ __device__ __forceinline__ Smem carve_smem(uint8_t *base, const Layout &L)
     Smem s;
     s.full = reinterpret_cast<uint64_t *>(base);
     s.empty = s.full + L.stages;
-    s.red = reinterpret_cast<float *>(base + 16 * 2 * 8);
+    s.red = reinterpret_cast<float *>(base + 16 * 2 * 8); // 256 B of barriers first
     s.flag = reinterpret_cast<int *>(base + kMiscBytes - 16);
-    s.ring = base + kMiscBytes;
+    s.wsm = reinterpret_cast<float *>(base + kMiscBytes);
+    s.ring = base + kMiscBytes + weight_smem_bytes(L.H);
     s.tens_bytes = (uint32_t)L.groups * L.H * 2;
     s.stage_bytes = s.tens_bytes * L.ntens;
     return s;
@@ -88,11 +90,11 @@ __device__ __forceinline__ void produce(const Smem &s, const Layout &L, const Ch
     const uint32_t row_bytes = (uint32_t)L.H * 2;
     bool ok = true;
     uint32_t it = 0;
+    uint32_t st = 0, ph = 0; // ring slot of tile `it` and the parity of its round
     for (; it < c.ntiles; ++it) {
-        const uint32_t st = it % L.stages;
         if (it >= (uint32_t)L.stages) {
-            const uint32_t par = ((it / L.stages) - 1) & 1;
-            bool got = mbar_wait(smem_addr(&s.empty[st]), par);
+            // the previous round of this slot was released by the consumers
+            bool got = mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u);
             got = __all_sync(0xffffffffu, got);
             if (!got) {
                 if (lane == 0)
@@ -124,6 +126,10 @@ __device__ __forceinline__ void produce(const Smem &s, const Layout &L, const Ch
                              full_bar, pol);
             }
         }
+        if (++st == (uint32_t)L.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
     }
     // Never leave copies in flight: wait (bounded) for the last issued stages.
     const uint32_t issued = it;
@@ -137,9 +143,11 @@ __device__ __forceinline__ void produce(const Smem &s, const Layout &L, const Ch
     (void)ok;
 }
 
-// Per-row group reduction: warp butterfly, then (W > 1) a fixed-order sum of
-// the W warp partials.  `abort` is OR-ed across the group.  `slot` toggles
-// per row so one barrier per row suffices.
+// Per-row group reduction: a warp butterfly, then (W > 1) lane i of every
+// warp of the group reads warp i's partial and a second butterfly sums them
+// (zeros past W), so every warp of the group ends with the same value in the
+// same fixed order.  `abort` is OR-ed across the group.  `slot` toggles per
+// row, so one barrier per row suffices.
 __device__ __forceinline__ float group_sum(float v, const Smem &s, const Layout &L, int gid,
                                            int wig, int lane, uint32_t slot, bool &abort)
 {
@@ -153,10 +161,7 @@ __device__ __forceinline__ float group_sum(float v, const Smem &s, const Layout 
     if (lane == 0)
         red[wig] = v;
     abort = named_sync_or(1 + gid, 32 * W, abort);
-    float t = 0.f;
-    for (int w = 0; w < W; ++w)
-        t += red[w];
-    return t;
+    return warp_sum(lane < W ? red[lane] : 0.f);
 }
 
 __device__ __forceinline__ void consumer_sync(const Layout &L)
@@ -164,30 +169,33 @@ __device__ __forceinline__ void consumer_sync(const Layout &L)
     named_sync(kConsumerBarrier, 32 * L.groups * L.warps_per_row);
 }
 
-// Load this thread's VPT vectors of w as FP32 (zeros past the row end).
-template <int VPT>
-__device__ __forceinline__ void load_weight(const void *w, int w_f32, int nvec, int gtid, int W,
-                                            float (&wf)[VPT][8])
+// Consumer threads stage w (BF16 or FP32) into shared memory as FP32, then
+// sync among themselves; the producer warp does not take part.  Two planes:
+// plane 0 holds columns 0-3 of every 8-column vector, plane 1 columns 4-7, so
+// that a warp reading its vectors' weights with 16-byte loads touches
+// consecutive addresses (no bank conflicts).
+__device__ __forceinline__ void stage_weight(const Smem &s, const Layout &L, const void *w, int w_f32)
 {
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = k * 32 * W + gtid;
-        if (v < nvec) {
-            if (w_f32) {
-                const float4 *p = reinterpret_cast<const float4 *>(w) + 2 * v;
-                float4 a = p[0], b = p[1];
-                wf[k][0] = a.x; wf[k][1] = a.y; wf[k][2] = a.z; wf[k][3] = a.w;
-                wf[k][4] = b.x; wf[k][5] = b.y; wf[k][6] = b.z; wf[k][7] = b.w;
-            } else {
-                uint4 u = reinterpret_cast<const uint4 *>(w)[v];
-                unpack8(u, wf[k]);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                wf[k][e] = 0.f;
-        }
+    const int nthr = 32 * L.groups * L.warps_per_row;
+    const int half = L.nvec * 4;
+    for (int j = threadIdx.x; j < L.H; j += nthr) {
+        const float v = w_f32 ? static_cast<const float *>(w)[j]
+                              : __uint_as_float((uint32_t)static_cast<const uint16_t *>(w)[j] << 16);
+        const int vec = j >> 3, e = j & 7;
+        s.wsm[(e >> 2) * half + vec * 4 + (e & 3)] = v;
     }
+    consumer_sync(L);
+}
+
+// The 8 weights of vector v as four FP32 pairs.
+__device__ __forceinline__ void weight_pairs(const Smem &s, const Layout &L, int v, float2 (&w2)[4])
+{
+    const float4 a = reinterpret_cast<const float4 *>(s.wsm)[v];
+    const float4 b = reinterpret_cast<const float4 *>(s.wsm)[L.nvec + v];
+    w2[0] = make_float2(a.x, a.y);
+    w2[1] = make_float2(a.z, a.w);
+    w2[2] = make_float2(b.x, b.y);
+    w2[3] = make_float2(b.z, b.w);
 }
 
 __device__ __forceinline__ int64_t out_off(int64_t st, int64_t sh, int64_t row_stride, int uniform,

@@ -176,8 +176,9 @@ typedef enum {
     CAKE_DW_PLAIN = 0,  /* FP32 running sum */
     CAKE_DW_BLOCKED = 1, /* FP32 sums over blocks of rows, folded into a
                             compensated (hi, lo) pair */
-    CAKE_DW_TWOSUM = 2  /* error-free TwoSum per element, with the product's
+    CAKE_DW_TWOSUM = 2, /* error-free TwoSum per element, with the product's
                             rounding error kept as well */
+    CAKE_DW_KAHAN = 3   /* Kahan-compensated FP32 sum of the rounded products */
 } cake_dw_accum;
 
 typedef struct {
@@ -240,6 +241,18 @@ cake_status cake_rmsnorm_bwd_noalloc(const cake_shape *shape, const cake_tensor 
                                      const cake_tensor *x, const float *rstd, const void *w,
                                      cake_dtype w_dtype, const cake_tensor *dh,
                                      const cake_tensor *dx, float *dw, cake_stream_t stream);
+
+/*
+ * Diagnostics: for the kernel a call with these arguments would launch, the
+ * CTAs per SM the table plans for (*planned) and the number the CUDA runtime
+ * reports can be resident (*resident).  backward = 0 asks about the forward
+ * (has_extra: with residual); backward = 1 about the backward (has_extra:
+ * with dh; deterministic and force_accum as in cake_rmsnorm_bwd_select).
+ * A plan asks for no more CTAs than fit, so *planned <= *resident.
+ */
+cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, int has_extra,
+                                        int deterministic, int force_accum, int *planned,
+                                        int *resident);
 
 /* ---- status ------------------------------------------------------------ */
 

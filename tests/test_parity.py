@@ -143,7 +143,7 @@ def test_fwd_empty(cake):
 
 # --------------------------------------------------------------------- bwd
 
-VARIANTS = [(0, tol_acc) for tol_acc in (0, 1, 2)] + [(1, tol_acc) for tol_acc in (0, 1, 2)]
+VARIANTS = [(0, acc) for acc in (0, 1, 2, 3)] + [(1, acc) for acc in (0, 1, 2, 3)]
 
 
 def oracle_bwd_inputs(x, w, eps, residual=None):
@@ -278,5 +278,19 @@ def test_single_kernel_leaves_workspace_clean(cake):
             first = dw.clone()
         # FP64 accumulation: repeated calls agree to FP32 rounding of the same sum
         assert torch.allclose(dw, first, rtol=1e-6, atol=1e-6)
-    head = ws[: 256 + 2048 * 8].cpu()
+    head = ws[: 256 + 8 * 2048 * 8].cpu()  # arrival counter and the 8 accumulator banks
     assert not head.any()
+
+
+@pytest.mark.parametrize("H", [8, 256, 512, 1536, 2048, 4096, 5120, 6144, 8192])
+def test_table_plans_only_resident_ctas(cake, H):
+    # every CTA of a plan's grid is resident at once: the table never asks for
+    # more CTAs per SM than the register file and shared memory hold
+    for backward in (False, True):
+        for extra in (False, True):
+            for det in (True, False):
+                for accum in (None, 0, 1, 2, 3):
+                    if not backward and (accum is not None or not det):
+                        continue
+                    planned, resident = cake.cake_rmsnorm_plan_occupancy((65536, 1, H), backward, extra, det, accum)
+                    assert 1 <= planned <= resident, (H, backward, extra, det, accum, planned, resident)

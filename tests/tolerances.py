@@ -42,12 +42,13 @@ U32 = 2.0 ** -24
 
 
 def dx_allowance(dy: np.ndarray, h: np.ndarray, w: np.ndarray, rstd: np.ndarray) -> np.ndarray:
-    """FP32 evaluation bound of rs*(g - xhat*c) for every element of [R, H] rows.
+    """FP32 evaluation bound of dx = (dy*w)*rs - h*kk, kk = rs^3 * c', for
+    every element of [R, H] rows (the kernel's order of operations).
 
-    g = dy*w and xhat = h*rs are rounded once each; c is a sum of H products
-    whose rounding error is at most 64*u*sum|g*xhat|/H (an FMA chain of 8 per
-    vector, the vectors of a thread, a 5-level butterfly and at most 24 warp
-    partials); the difference and the final product add 2u each.
+    g = dy*w is rounded once; kk carries the roundings of rs*rs, *rs, the sum
+    c' = (1/H) sum g*h (at most 64*u*sum|g*h|/H: an FMA chain per thread, a
+    5-level butterfly, at most 24 warp partials) and the products, about 6u
+    relative in all, then h*kk and the final FMA round once more each.
     """
     rs = rstd.astype(np.float64)[:, None]
     g = dy * w[None, :]
@@ -56,7 +57,7 @@ def dx_allowance(dy: np.ndarray, h: np.ndarray, w: np.ndarray, rstd: np.ndarray)
     c = (g * xh).sum(axis=1, keepdims=True) / H
     dc = 64 * U32 * np.abs(g * xh).sum(axis=1, keepdims=True) / H
     t = g - xh * c
-    return rs * (2 * U32 * (np.abs(g) + np.abs(xh * c) + np.abs(t)) + np.abs(xh) * dc)
+    return rs * (2 * U32 * (np.abs(g) + np.abs(t)) + 8 * U32 * np.abs(xh * c) + np.abs(xh) * dc)
 
 
 def dx_check(dx_bits: np.ndarray, dx64: np.ndarray, dy: np.ndarray, h: np.ndarray, w: np.ndarray,
