@@ -51,7 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["det", "nondet", "fwd", "all"], default=None,
+    ap.add_argument("--profile", choices=["det", "nondet", "fwd", "main", "all"], default=None,
                     help="run only the named loop(s) with few launches (for ncu); prints per-call times")
     ap.add_argument("--accum", choices=sorted(ACCUM), default=None,
                     help="with --profile: force the per-thread dw accumulation form")
@@ -226,6 +226,18 @@ def time_loop(torch, fn, steps, warmup, flush, stream):
 
 # ---------------------------------------------------------- our CUDA path
 
+def describe(spec) -> str:
+    kind = spec["kind"]
+    wd = "w FP32" if spec["w_dtype"] is not None and str(spec["w_dtype"]).endswith("float32") else "w BF16"
+    if kind == "plain":
+        fam = {"gauss": "N(0,1)", "outlier": "N(0,1), 1% rows x30", "offset": "3+N(0,1)"}[spec["family"]]
+        return f"x BF16 {fam}; dy BF16 N(0, std {spec['dy_std']:g}); {wd} 1+0.1N(0,1); eps 1e-6"
+    if kind == "res":
+        return f"x BF16 N(0,1), residual N(0, std 0.5), dy and dh BF16 N(0,1); {wd} 1+0.1N(0,1); eps 1e-6"
+    view = "strided slice of [T,24,512]" if spec.get("strided") else "contiguous"
+    return f"[T,{spec['heads']},256] {view}, x 3+N(0,1), dy N(0,1); shared {wd}[256]; eps 1e-6"
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -245,16 +257,19 @@ def run_ours(args):
     import cake_inputs
 
     spec = cake_inputs.WORKLOADS[args.workload]
-    if spec["kind"] != "plain":
-        raise SystemExit("the headline bench runs plain [T, H] workloads; use --profile for the others")
-    T, H = spec["T"], spec["H"]
     case = cake_inputs.make(args.workload, seed=rank, device=dev)
     x, dy, w = case["x"], case["dy"], case["w"]
+    dh, res = case.get("dh"), case.get("residual")
     fns = make_step_fns(cake, torch, case, dev)
-    rstd, ws, dx, dw = fns["rstd"], fns["ws"], fns["dx"], fns["dw"]
-    variant = cake.cake_rmsnorm_bwd_select((T, 1, H), w.dtype, deterministic=True)
-    nd_variant = cake.cake_rmsnorm_bwd_select((T, 1, H), w.dtype, deterministic=False)
-    nbytes = workload_bytes(T, H, w.numel() * w.element_size(), variant["ctas"])
+    h, rstd, ws, dx, dw = fns["h"], fns["rstd"], fns["ws"], fns["dx"], fns["dw"]
+    T = x.shape[0]
+    nh = x.shape[1] if x.dim() == 3 else 1
+    H = x.shape[-1]
+    R = T * nh
+    variant = cake.cake_rmsnorm_bwd_select((T, nh, H), w.dtype, deterministic=True, has_dh=dh is not None)
+    nd_variant = cake.cake_rmsnorm_bwd_select((T, nh, H), w.dtype, deterministic=False, has_dh=dh is not None)
+    nbytes = workload_bytes(R, H, w.numel() * w.element_size(), variant["ctas"], dh=dh is not None,
+                            res=res is not None)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     K, Wm = args.steps, max(3, args.warmup)
@@ -270,23 +285,36 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks = clk.summary()
 
-    # end to end through the C ABI from pinned host buffers
-    hx, hdy, hrstd, hw = (t.cpu().pin_memory() for t in (x, dy, rstd, w))
-    hdx = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
+    # end to end through the C ABI from pinned host buffers: every step copies
+    # the backward's inputs in and dx, dw out
+    def host(t):
+        if t is None:
+            return None
+        if not t.is_contiguous():  # a strided view travels as its whole buffer
+            t = t.as_strided((t.untyped_storage().nbytes() // t.element_size(),), (1,), 0)
+        return t.cpu().pin_memory()
+
+    hx, hdy, hdh, hrstd, hw = (host(t) for t in (h, dy, dh, rstd, w))
+    hdx = torch.empty(dx.shape, dtype=torch.bfloat16).pin_memory()
     hdw = torch.empty(H, dtype=torch.float32).pin_memory()
-    dx2, dy2, x2, r2, w2 = (torch.empty_like(t) for t in (dx, dy, x, rstd, w))
+    bx = torch.empty(hx.shape, dtype=hx.dtype, device=dev)
+    x2 = bx if h.is_contiguous() else bx.as_strided(h.shape, h.stride(), h.storage_offset())
+    dy2, r2, w2, dx2 = (torch.empty_like(t) for t in (dy, rstd, w, dx))
+    dh2 = torch.empty_like(dh) if dh is not None else None
 
     def e2e_step():
-        x2.copy_(hx, non_blocking=True)
+        bx.copy_(hx, non_blocking=True)
         dy2.copy_(hdy, non_blocking=True)
+        if dh2 is not None:
+            dh2.copy_(hdh, non_blocking=True)
         r2.copy_(hrstd, non_blocking=True)
         w2.copy_(hw, non_blocking=True)
-        cake.cake_rmsnorm_bwd(dy2, x2, r2, w2, deterministic=True, workspace=ws, dx=dx2, dw=dw)
+        cake.cake_rmsnorm_bwd(dy2, x2, r2, w2, dh2, deterministic=True, workspace=ws, dx=dx2, dw=dw)
         hdx.copy_(dx2, non_blocking=True)
         hdw.copy_(dw, non_blocking=True)
 
     t_e2e = time_loop(torch, e2e_step, K, Wm, flush, stream)
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hdy, hrstd, hw))
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hdy, hdh, hrstd, hw) if t is not None)
     d2h = hdx.numel() * 2 + hdw.numel() * 4
     assert cake.cake_rmsnorm_device_status() == 0
 
@@ -305,7 +333,7 @@ def run_ours(args):
     gbs = lambda b, tot_ms: world * K * b / (tot_ms * 1e-3) / 1e9
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and spec["kind"] == "plain":
         cpu = oracle_baseline(case, T, H, budget_s=10.0)
     if world > 1:
         dist.barrier()
@@ -333,11 +361,11 @@ def run_ours(args):
         "impl": "ours",
         "config": {
             "workload": args.workload,
-            "T": T, "H": H, "w_dtype": "fp32" if w.dtype == torch.float32 else "bf16",
-            "inputs": "x BF16 N(0,1), 1% rows x30; dy BF16 N(0, std 1e-2); w FP32 1+0.1N(0,1); eps 1e-6",
+            "T": T, "heads": nh, "H": H, "w_dtype": "fp32" if w.dtype == torch.float32 else "bf16",
+            "inputs": describe(spec),
             "mode": "deterministic (main + fixed-order reduce)",
             "io_dtype": "bf16 activations, fp32 rstd/dw",
-            "l2": "flushed before every timed step (256 MiB write); working set 805 MB > L2",
+            "l2": "flushed before every timed step (256 MiB write)",
             "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
             "variant": variant,
         },
@@ -349,8 +377,8 @@ def run_ours(args):
                          "bytes": nbytes["pair"]},
             "det_main_kernel": {"us": round(mean_main * 1e3, 2), "GB/s": round(achieved_main, 1),
                                 "bytes": nbytes["main"]},
-            "nondet_single": {"us": round(mean_nd * 1e3, 2), "GB/s": round(gbs(nbytes["single"], tot_nd), 1),
-                              "bytes": nbytes["single"], "variant": nd_variant},
+            "nondet": {"us": round(mean_nd * 1e3, 2), "GB/s": round(gbs(nbytes["single"], tot_nd), 1),
+                       "bytes": nbytes["single"], "variant": nd_variant},
             "fwd": {"us": round(mean_fwd * 1e3, 2), "GB/s": round(gbs(nbytes["fwd"], tot_fwd), 1),
                     "bytes": nbytes["fwd"]},
         },
@@ -372,8 +400,9 @@ def run_ours(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
         },
-        "gpu_launches": K * (2 + 1 + 1 + 1 + 2),
-        "gpu_launches_detail": {"det": 2 * K, "main_only": K, "nondet": K, "fwd": K, "e2e": 2 * K},
+        "gpu_launches": K * (2 + 1 + (1 if nd_variant["single"] else 2) + 1 + 2),
+        "gpu_launches_detail": {"det": 2 * K, "main_only": K, "nondet": K * (1 if nd_variant["single"] else 2),
+                                "fwd": K, "e2e": 2 * K},
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

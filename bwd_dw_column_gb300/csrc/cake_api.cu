@@ -63,7 +63,7 @@ enum Kind { kFwd = 0, kBwd = 1 };
 // bits of dx / y / rstd; a different cps or groups changes the pair's
 // partition and therefore the bits of the deterministic dw.
 struct Tune {
-    int v[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages]
+    int v[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages, rpg, form+1]
 };
 
 static Tune parse_tune(const char *t)
@@ -71,7 +71,8 @@ static Tune parse_tune(const char *t)
     Tune r;
     if (!t)
         return r;
-    static const char *keys[2][4] = {{"fvpt", "fgroups", "fcps", "fstages"}, {"vpt", "groups", "cps", "stages"}};
+    static const char *keys[2][6] = {{"fvpt", "fgroups", "fcps", "fstages", "frpg", "fform"},
+                                     {"vpt", "groups", "cps", "stages", "rpg", "form"}};
     const char *p = t;
     while (*p) {
         const char *eq = strchr(p, '=');
@@ -80,9 +81,9 @@ static Tune parse_tune(const char *t)
         const size_t klen = (size_t)(eq - p);
         const int val = atoi(eq + 1);
         for (int k = 0; k < 2; ++k)
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 6; ++i)
                 if (strlen(keys[k][i]) == klen && strncmp(p, keys[k][i], klen) == 0)
-                    r.v[k][i] = val;
+                    r.v[k][i] = i == 5 ? val + 1 : val;
         const char *comma = strchr(eq, ',');
         if (!comma)
             break;
@@ -129,7 +130,9 @@ static RowLayout row_layout(int H, Kind kind)
         return {1, 1};
     if (kind == kBwd && nvec <= 32 * 24)
         return layout_for(H, 1);
-    for (int vpt = 2; vpt <= 4; ++vpt) {
+    // forward: 16 columns per thread up to H = 4096, then 24 (measured on
+    // GB300: H = 6144 runs 7 % faster with 24 than with 16)
+    for (int vpt = nvec <= 512 ? 2 : 3; vpt <= 4; ++vpt) {
         RowLayout l = layout_for(H, vpt);
         if ((l.W + 1) * 32 <= kMaxThreadsFor(vpt))
             return l;
@@ -139,30 +142,37 @@ static RowLayout row_layout(int H, Kind kind)
 
 struct Plan {
     RowLayout rl;
-    int groups, stages, ctas_per_sm, ctas;
+    int groups, rpg, stages, ctas_per_sm, ctas;
     uint32_t rows_per_cta;
     size_t smem;
     int single, dwm;
 };
 
-static size_t ring_smem(int ntens, int groups, int H, int stages)
+static size_t ring_smem(int ntens, int rows_per_stage, int H, int stages)
 {
-    return (size_t)kMiscBytes + weight_smem_bytes(H) + (size_t)stages * ntens * groups * H * 2;
+    return (size_t)kMiscBytes + weight_smem_bytes(H) + (size_t)stages * ntens * rows_per_stage * H * 2;
 }
 
 // Registers per thread of each row kernel as compiled for sm_103a (ptxas
 // -v), by kind and VPT; the resident-CTA count below follows from them and
 // a GPU test checks it against the occupancy the runtime reports.
-static int kernel_regs(Kind kind, int vpt)
+static int kernel_regs(Kind kind, int vpt, int rpg, int dwm)
 {
-    static const int bwd[5] = {0, 72, 128, 128, 128};
     static const int fwd[5] = {0, 48, 64, 80, 96};
-    return kind == kBwd ? bwd[vpt] : fwd[vpt];
+    if (kind == kFwd)
+        return fwd[vpt];
+    if (vpt == 1 && rpg == 2) {
+        static const int r2[4] = {104, 120, 128, 112}; // plain, blocked, twosum, kahan
+        return r2[dwm & 3];
+    }
+    if (vpt == 1)
+        return dwm == CAKE_DW_PLAIN ? 64 : 72;
+    return 128;
 }
 
-static int resident_limit(Kind kind, int vpt, int warps_per_cta)
+static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int warps_per_cta)
 {
-    const int regs = (kernel_regs(kind, vpt) + 7) & ~7;
+    const int regs = (kernel_regs(kind, vpt, rpg, dwm) + 7) & ~7;
     const int by_regs = 65536 / (warps_per_cta * 32 * regs);
     const int by_warps = 64 / warps_per_cta;
     return by_regs < by_warps ? by_regs : by_warps;
@@ -171,32 +181,53 @@ static int resident_limit(Kind kind, int vpt, int warps_per_cta)
 // Per-H CTA shape: row groups (rows in flight) per CTA and CTAs per SM.
 // About 8 consumer warps per CTA where the row allows it, then as many CTAs
 // per SM as the register file holds (at most 3).
-static void cta_shape(const RowLayout &rl, Kind kind, int &groups, int &ctas_per_sm)
+static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &groups, int &ctas_per_sm)
 {
     const int W = rl.W;
-    const int max_warps = kMaxThreadsFor(rl.vpt) / 32 - 1; // consumer warps per CTA
+    const int max_warps = (rpg == 2 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
     groups = W >= 8 ? 1 : 8 / W;
     const Tune &t = tune();
     if (t.v[kind][1] > 0)
         groups = t.v[kind][1];
     while (groups * W > max_warps && groups > 1)
         --groups;
-    ctas_per_sm = resident_limit(kind, rl.vpt, groups * W + 1);
-    if (ctas_per_sm > 3)
-        ctas_per_sm = 3;
+    ctas_per_sm = resident_limit(kind, rl.vpt, rpg, dwm, groups * W + 1);
+    // at most 3 resident CTAs; the forward's warp-per-row layout takes 4,
+    // and its 4-warps-per-row layout runs best at 2 (GB300 measurements)
+    int cap = 3;
+    if (kind == kFwd && W == 1)
+        cap = 4;
+    else if (kind == kFwd && W > 1 && W <= 4)
+        cap = 2;
+    if (ctas_per_sm > cap)
+        ctas_per_sm = cap;
     if (ctas_per_sm < 1)
         ctas_per_sm = 1;
     if (t.v[kind][2] > 0)
         ctas_per_sm = t.v[kind][2];
 }
 
+// Rows a row group owns per stage: two (interleaved reductions, one barrier)
+// where the table says so, for the backward with 8 columns per thread.
+static int rows_per_group(const RowLayout &rl, Kind kind)
+{
+    int rpg = 1;
+    const int forced = tune().v[kind][4];
+    if (forced == 1 || forced == 2)
+        rpg = forced;
+    if (kind != kBwd || rl.vpt != 1 || rl.W > 8)
+        rpg = 1;
+    return rpg;
+}
+
 static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, int dwm)
 {
     Plan p;
     p.rl = row_layout(H, kind);
-    cta_shape(p.rl, kind, p.groups, p.ctas_per_sm);
+    p.rpg = rows_per_group(p.rl, kind);
+    cta_shape(p.rl, kind, p.rpg, dwm, p.groups, p.ctas_per_sm);
     const size_t per_cta = kSmemPerSM / p.ctas_per_sm;
-    const size_t stage = (size_t)ntens * p.groups * H * 2;
+    const size_t stage = (size_t)ntens * p.groups * p.rpg * H * 2;
     const size_t fixed = (size_t)kMiscBytes + weight_smem_bytes(H);
     int stages = per_cta > fixed ? (int)((per_cta - fixed) / stage) : 0;
     if (tune().v[kind][3] >= 2 && tune().v[kind][3] < stages)
@@ -210,12 +241,12 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
             stages = kMaxStages;
     }
     p.stages = stages;
-    p.smem = ring_smem(ntens, p.groups, H, stages);
+    p.smem = ring_smem(ntens, p.groups * p.rpg, H, stages);
     // the group-combine buffer reuses the ring
     const size_t comb = fixed + (size_t)(p.groups > 1 ? p.groups - 1 : 0) * H * 8;
     if (comb > p.smem)
         p.smem = comb;
-    const uint32_t tile = (uint32_t)p.groups;
+    const uint32_t tile = (uint32_t)(p.groups * p.rpg);
     const uint32_t max_ctas = (uint32_t)kSMs * p.ctas_per_sm;
     uint32_t ctas = rows == 0 ? 0 : (rows + tile - 1) / tile; // at least one tile per CTA
     if (ctas > max_ctas)
@@ -261,6 +292,18 @@ static size_t ws_part_off(int H) { return align256(kWsHeader + (size_t)kAccBanks
 static size_t ws_size(int H, int ctas, int need_partials)
 {
     return ws_part_off(H) + (need_partials ? (size_t)ctas * H * 8 : 0);
+}
+static int tree_groups(int ctas) { return (ctas + kTreeGroup - 1) / kTreeGroup; }
+static size_t ws_tree_off(int H, int ctas) { return align256(ws_size(H, ctas, 1)); }
+// Bytes each form needs: the atomic single kernel its counter and one bank,
+// the pair its partials, the tree its partials and the group totals.
+static size_t ws_need(int form, int H, int ctas)
+{
+    if (form == kFormAtomic)
+        return kWsHeader + (size_t)H * 8;
+    if (form == kFormTree)
+        return ws_tree_off(H, ctas) + (size_t)tree_groups(ctas) * H * 8;
+    return ws_size(H, ctas, 1);
 }
 
 } // namespace cake
@@ -340,6 +383,7 @@ Layout make_layout(const Plan &p, int H, uint32_t rows, uint32_t nh, int ntens)
     L.nvec = H / 8;
     L.warps_per_row = p.rl.W;
     L.groups = p.groups;
+    L.rows_per_group = p.rpg;
     L.stages = p.stages;
     L.ntens = ntens;
     L.rows = rows;
@@ -356,6 +400,7 @@ void fill_variant(const Plan &p, cake_variant *out)
     out->vec_per_thread = p.rl.vpt;
     out->warps_per_row = p.rl.W;
     out->row_groups = p.groups;
+    out->rows_per_group = p.rpg;
     out->stages = p.stages;
     out->ctas = p.ctas;
     out->rows_per_cta = p.rows_per_cta;
@@ -368,17 +413,22 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
     cake_status st = check_shape(shape, rows);
     if (st != CAKE_OK)
         return st;
-    if (force_single > 1 || force_accum > CAKE_DW_KAHAN)
+    if (force_single > kFormTree || force_accum > CAKE_DW_KAHAN)
         return CAKE_ERR_INVALID;
-    if (deterministic && force_single == 1)
+    if (deterministic && force_single == kFormAtomic)
         return CAKE_ERR_INVALID;
     int single, dwm;
     pick_variant(*rows, deterministic, single, dwm);
+    if (tune().v[kBwd][5] > 0 && (tune().v[kBwd][5] - 1 != kFormAtomic || !deterministic))
+        single = tune().v[kBwd][5] - 1;
     if (force_single >= 0)
         single = force_single;
     if (force_accum >= 0)
         dwm = force_accum;
     *plan = make_plan((int)shape->hidden, *rows, has_dh ? 3 : 2, kBwd, single, dwm);
+    if (plan->single == kFormTree &&
+        (plan->rl.vpt != 1 || plan->rpg != 1 || tree_groups(plan->ctas) > (int)(kWsHeader / 4) - 2))
+        return CAKE_ERR_UNSUPPORTED;
     return CAKE_OK;
 }
 
@@ -415,7 +465,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
         return st;
     if (has_dh && (st = check_tensor(dh, shape)) != CAKE_OK)
         return st;
-    const size_t need = plan.single ? kWsHeader + (size_t)H * 8 : ws_size(H, plan.ctas, 1);
+    const size_t need = ws_need(plan.single, H, plan.ctas);
     if (!workspace || workspace_bytes < need)
         return CAKE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -440,6 +490,8 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.arrivals = reinterpret_cast<unsigned int *>(ws);
     p.acc = reinterpret_cast<double *>(ws + ws_acc_off());
     p.partials = reinterpret_cast<float2 *>(ws + ws_part_off(H));
+    p.tree_cnt = reinterpret_cast<unsigned int *>(ws) + 1;
+    p.group_totals = reinterpret_cast<float2 *>(ws + ws_tree_off(H, plan.ctas));
     // the accumulator banks that fit the given workspace (the built-in
     // scratch of the allocation-free entry point may hold fewer than 8)
     {
@@ -449,7 +501,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.block_rows = 16;
     p.status = nullptr;
     cudaError_t e = launch_bwd_rows(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s);
-    if (e != cudaSuccess || plan.single || phase == kMainOnly)
+    if (e != cudaSuccess || plan.single != kFormPair || phase == kMainOnly)
         return cuda_status(e);
     ReduceParams rp{p.partials, plan.ctas, H, dw, reduce_slices(H)};
     return cuda_status(launch_dw_reduce(rp, s));
@@ -611,12 +663,13 @@ size_t cake_rmsnorm_bwd_workspace_size(const cake_shape *shape, cake_dtype w_dty
     // the largest of every variant this mode may run (the table or a forced one)
     const int H = (int)shape->hidden;
     size_t need = 0;
-    for (int ntens = 2; ntens <= 3; ++ntens) {
-        Plan p = make_plan(H, rows, ntens, kBwd, 0, 0);
-        size_t n = ws_size(H, p.ctas, 1);
-        if (n > need)
-            need = n;
-    }
+    for (int ntens = 2; ntens <= 3; ++ntens)
+        for (int dwm = CAKE_DW_PLAIN; dwm <= CAKE_DW_KAHAN; ++dwm) {
+            Plan p = make_plan(H, rows, ntens, kBwd, 0, dwm);
+            size_t n = ws_need(kFormTree, H, p.ctas);
+            if (n > need)
+                need = n;
+        }
     (void)deterministic;
     return need;
 }
@@ -673,7 +726,7 @@ cake_status cake_rmsnorm_bwd_main(const cake_shape *shape, const cake_tensor *dy
                                   void *workspace, size_t workspace_bytes, int force_accum,
                                   cake_stream_t stream)
 {
-    return run_bwd(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, workspace, workspace_bytes, 1, 0,
+    return run_bwd(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, workspace, workspace_bytes, 1, kFormPair,
                    force_accum, stream, kMainOnly);
 }
 
@@ -722,7 +775,7 @@ cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, i
         return st;
     const int threads = 32 * (plan.groups * plan.rl.W + 1);
     int n = 0;
-    cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.single, plan.dwm, threads, plan.smem, &n)
+    cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.rpg, plan.single, plan.dwm, threads, plan.smem, &n)
                              : occupancy_fwd(plan.rl.vpt, threads, plan.smem, &n);
     if (e != cudaSuccess)
         return CAKE_ERR_CUDA;

@@ -58,8 +58,9 @@ static cudaError_t status_ptr(int **out)
     return cudaSuccess;
 }
 
-template <int VPT, int DWM, bool SINGLE>
-__global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) bwd_rows_kernel(const __grid_constant__ BwdParams p)
+template <int VPT, int DWM, int FORM, int R2>
+__global__ void __launch_bounds__(R2 == 1 ? kMaxThreadsFor(VPT) : kMaxThreadsR2, 1)
+    bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const Layout &L = p.L;
@@ -101,120 +102,150 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) bwd_rows_kernel(const 
         }
     int blk_rows = 0;
 
-    auto rs_of_tile = [&](uint32_t tile) {
-        const uint32_t r = c.r0 + tile * c.tile_rows + gid;
+    // A group owns R2 consecutive rows of every tile: gid*R2 + i.
+    auto rs_of = [&](uint32_t tile, int i) {
+        const uint32_t r = c.r0 + tile * c.tile_rows + gid * R2 + i;
         return (tile < c.ntiles && r < c.r_end) ? __ldg(p.rstd + r) : 0.f;
     };
-    // rstd of this group's row, loaded four tiles ahead (a register ring)
-    float rs_cur = rs_of_tile(0), rs_n1 = rs_of_tile(1), rs_n2 = rs_of_tile(2), rs_n3 = rs_of_tile(3);
+    // rstd of this group's rows, loaded kAhead tiles ahead (a register ring)
+    constexpr int kAhead = R2 == 1 ? 4 : 2;
+    float rsr[kAhead][R2];
+#pragma unroll
+    for (int d = 0; d < kAhead; ++d)
+#pragma unroll
+        for (int i = 0; i < R2; ++i)
+            rsr[d][i] = rs_of(d, i);
 
     bool abort = false;
     uint32_t slot = 0;
     uint32_t st = 0, ph = 0; // ring slot of tile `it` and the parity of its round
     for (uint32_t it = 0; it < c.ntiles && !abort; ++it) {
-        const float rs_n4 = rs_of_tile(it + 4);
+        float rsn[R2];
+#pragma unroll
+        for (int i = 0; i < R2; ++i)
+            rsn[i] = rs_of(it + kAhead, i);
         abort = !mbar_wait(smem_addr(&s.full[st]), ph);
         const uint8_t *stage = s.ring + st * s.stage_bytes;
-        const uint32_t r = c.r0 + it * c.tile_rows + gid;
-        if (r < c.r_end) { // uniform across the group
-            const float rs = rs_cur;
-            const float2 rs2 = make_float2(rs, rs);
-            const float2 nrs2 = make_float2(-rs, -rs);
-            const uint4 *xs = reinterpret_cast<const uint4 *>(stage + gid * L.H * 2);
-            const uint4 *dys = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + gid * L.H * 2);
-            const uint4 *dhs = reinterpret_cast<const uint4 *>(stage + 2 * s.tens_bytes + gid * L.H * 2);
-
-            // One pass over the staged row: m = dy*w and the row dot
-            // sum m*h (even / odd columns in the two lanes, in the order of
-            // k and q; then lane 0 + lane 1; then the group reduction), and
-            // the dw terms dy*h*rstd (dy*h is exact in FP32).
+        const uint32_t rbase = c.r0 + it * c.tile_rows + gid * R2;
+        const int nrow = rbase < c.r_end ? (int)min((uint32_t)R2, c.r_end - rbase) : 0; // uniform in the group
+        if (nrow > 0) {
+            // One pass over each staged row: m = dy*w and the row dot sum m*h
+            // (even / odd columns in the two lanes, in the order of k and q;
+            // then lane 0 + lane 1; then the group reduction), and the dw
+            // terms dy*h*rstd (dy*h is exact in FP32), rows in order.
             // VPT == 1 keeps x and m in registers for the dx step; wider
-            // layouts re-read the staged row instead (fewer registers)
+            // layouts re-read the staged row instead (fewer registers).
             constexpr bool kKeep = VPT == 1;
-            float2 x2[kKeep ? VPT : 1][4], m2[kKeep ? VPT : 1][4];
-            float2 dot2 = make_float2(0.f, 0.f);
+            float2 x2[R2][kKeep ? VPT : 1][4], m2[R2][kKeep ? VPT : 1][4];
+            float dot[R2];
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                uint4 xr = make_uint4(0, 0, 0, 0), dr = make_uint4(0, 0, 0, 0);
-                if (v < nvec) {
-                    xr = xs[v];
-                    dr = dys[v];
-                }
-                float2 w2[4];
-                weight_pairs(s, L, v < nvec ? v : 0, w2);
+            for (int i = 0; i < R2; ++i) {
+                dot[i] = 0.f;
+                if (i >= nrow)
+                    continue;
+                const int tr = gid * R2 + i;
+                const float rs = rsr[0][i];
+                const float2 rs2 = make_float2(rs, rs);
+                const float2 nrs2 = make_float2(-rs, -rs);
+                const uint4 *xs = reinterpret_cast<const uint4 *>(stage + tr * L.H * 2);
+                const uint4 *dys = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + tr * L.H * 2);
+                float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 xv = bf2(word(xr, q));
-                    const float2 d2 = bf2(word(dr, q));
-                    const float2 mv = mul2(d2, w2[q]);
-                    if (kKeep) {
-                        x2[kKeep ? k : 0][q] = xv;
-                        m2[kKeep ? k : 0][q] = mv;
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = k * 32 * W + gtid;
+                    uint4 xr = make_uint4(0, 0, 0, 0), dr = make_uint4(0, 0, 0, 0);
+                    if (v < nvec) {
+                        xr = xs[v];
+                        dr = dys[v];
                     }
-                    dot2 = fma2(mv, xv, dot2);
-                    const float2 a2 = mul2(d2, xv);
-                    if (DWM == CAKE_DWM_PLAIN) {
-                        hi[k][q] = fma2(a2, rs2, hi[k][q]);
-                    } else if (DWM == CAKE_DWM_BLOCKED) {
-                        blk[k][q] = fma2(a2, rs2, blk[k][q]);
-                    } else if (DWM == CAKE_DWM_TWOSUM) {
-                        // npr = -RN(a*rs); pe = a*rs - RN(a*rs) exactly (FMA);
-                        // Knuth's TwoSum of hi and RN(a*rs) written with npr:
-                        // s = hi + pr, e = (hi - (s - (s - hi))) + (pr - (s - hi));
-                        // lo collects e and pe
-                        const float2 npr = mul2(a2, nrs2);
-                        const float2 pe = fma2(a2, rs2, npr);
-                        const float2 sm = sub2(hi[k][q], npr);
-                        const float2 bp = sub2(sm, hi[k][q]);
-                        const float2 ap = sub2(sm, bp);
-                        const float2 e = sub2(sub2(hi[k][q], ap), add2(npr, bp));
-                        hi[k][q] = sm;
-                        lo[k][q] = add2(lo[k][q], add2(e, pe));
-                    } else {
-                        // Kahan: lo holds the negated running compensation
-                        const float2 y = fma2(a2, rs2, lo[k][q]);
-                        const float2 t = add2(hi[k][q], y);
-                        lo[k][q] = add2(sub2(hi[k][q], t), y);
-                        hi[k][q] = t;
-                    }
-                }
-            }
-            const float dot = __fadd_rn(dot2.x, dot2.y);
-            const float tot = group_sum(dot, s, L, gid, wig, lane, slot++, abort);
-            // dx_j = rs*(g_j - xhat_j*c) = m_j*rs - h_j*kk, kk = rs^3 * tot / H
-            const float kk = __fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), __fmul_rn(tot, L.inv_h));
-            const float2 nk2 = make_float2(-kk, -kk);
-
-            uint16_t *dxrow = p.dx + out_off(p.dx_st, p.dx_sh, p.dx_row_stride, p.dx_uniform, r, L.nh);
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                if (v < nvec && !abort) {
-                    uint4 hv = make_uint4(0, 0, 0, 0);
-                    if (has_dh)
-                        hv = dhs[v];
-                    uint4 xr2 = make_uint4(0, 0, 0, 0), dr2 = make_uint4(0, 0, 0, 0);
                     float2 w2[4];
-                    if (!kKeep) {
-                        xr2 = xs[v];
-                        dr2 = dys[v];
-                        weight_pairs(s, L, v, w2);
-                    }
-                    uint32_t o[4];
+                    weight_pairs(s, L, v < nvec ? v : 0, w2);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const float2 xv = kKeep ? x2[kKeep ? k : 0][q] : bf2(word(xr2, q));
-                        const float2 mv = kKeep ? m2[kKeep ? k : 0][q] : mul2(bf2(word(dr2, q)), w2[q]);
-                        float2 d = fma2(mv, rs2, mul2(xv, nk2));
-                        if (has_dh)
-                            d = add2(d, bf2(word(hv, q)));
-                        o[q] = pack2(d);
+                        const float2 xv = bf2(word(xr, q));
+                        const float2 d2 = bf2(word(dr, q));
+                        const float2 mv = mul2(d2, w2[q]);
+                        if (kKeep) {
+                            x2[i][kKeep ? k : 0][q] = xv;
+                            m2[i][kKeep ? k : 0][q] = mv;
+                        }
+                        dot2 = fma2(mv, xv, dot2);
+                        const float2 a2 = mul2(d2, xv);
+                        if (DWM == CAKE_DWM_PLAIN) {
+                            hi[k][q] = fma2(a2, rs2, hi[k][q]);
+                        } else if (DWM == CAKE_DWM_BLOCKED) {
+                            blk[k][q] = fma2(a2, rs2, blk[k][q]);
+                        } else if (DWM == CAKE_DWM_TWOSUM) {
+                            // npr = -RN(a*rs); pe = a*rs - RN(a*rs) exactly (FMA);
+                            // Knuth's TwoSum of hi and RN(a*rs) written with npr:
+                            // s = hi + pr, e = (hi - (s - (s - hi))) + (pr - (s - hi));
+                            // lo collects e and pe
+                            const float2 npr = mul2(a2, nrs2);
+                            const float2 pe = fma2(a2, rs2, npr);
+                            const float2 sm = sub2(hi[k][q], npr);
+                            const float2 bp = sub2(sm, hi[k][q]);
+                            const float2 ap = sub2(sm, bp);
+                            const float2 e = sub2(sub2(hi[k][q], ap), add2(npr, bp));
+                            hi[k][q] = sm;
+                            lo[k][q] = add2(lo[k][q], add2(e, pe));
+                        } else {
+                            // Kahan: lo holds the negated running compensation
+                            const float2 y = fma2(a2, rs2, lo[k][q]);
+                            const float2 t = add2(hi[k][q], y);
+                            lo[k][q] = add2(sub2(hi[k][q], t), y);
+                            hi[k][q] = t;
+                        }
                     }
-                    __stcs(reinterpret_cast<uint4 *>(dxrow) + v, make_uint4(o[0], o[1], o[2], o[3]));
+                }
+                dot[i] = __fadd_rn(dot2.x, dot2.y);
+            }
+            float tot[R2];
+            group_sum_n<R2>(dot, tot, s, L, gid, wig, lane, slot++, abort);
+
+#pragma unroll
+            for (int i = 0; i < R2; ++i) {
+                if (i >= nrow)
+                    continue;
+                const int tr = gid * R2 + i;
+                const float rs = rsr[0][i];
+                const float2 rs2 = make_float2(rs, rs);
+                // dx_j = rs*(g_j - xhat_j*c) = m_j*rs - h_j*kk, kk = rs^3 * tot / H
+                const float kk = __fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), __fmul_rn(tot[i], L.inv_h));
+                const float2 nk2 = make_float2(-kk, -kk);
+                const uint4 *xs = reinterpret_cast<const uint4 *>(stage + tr * L.H * 2);
+                const uint4 *dys = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + tr * L.H * 2);
+                const uint4 *dhs = reinterpret_cast<const uint4 *>(stage + 2 * s.tens_bytes + tr * L.H * 2);
+                uint16_t *dxrow =
+                    p.dx + out_off(p.dx_st, p.dx_sh, p.dx_row_stride, p.dx_uniform, rbase + i, L.nh);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = k * 32 * W + gtid;
+                    if (v < nvec && !abort) {
+                        uint4 hv = make_uint4(0, 0, 0, 0);
+                        if (has_dh)
+                            hv = dhs[v];
+                        uint4 xr2 = make_uint4(0, 0, 0, 0), dr2 = make_uint4(0, 0, 0, 0);
+                        float2 w2[4];
+                        if (!kKeep) {
+                            xr2 = xs[v];
+                            dr2 = dys[v];
+                            weight_pairs(s, L, v, w2);
+                        }
+                        uint32_t o[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 xv = kKeep ? x2[i][kKeep ? k : 0][q] : bf2(word(xr2, q));
+                            const float2 mv = kKeep ? m2[i][kKeep ? k : 0][q] : mul2(bf2(word(dr2, q)), w2[q]);
+                            float2 d = fma2(mv, rs2, mul2(xv, nk2));
+                            if (has_dh)
+                                d = add2(d, bf2(word(hv, q)));
+                            o[q] = pack2(d);
+                        }
+                        __stcs(reinterpret_cast<uint4 *>(dxrow) + v, make_uint4(o[0], o[1], o[2], o[3]));
+                    }
                 }
             }
-            if (DWM == CAKE_DWM_BLOCKED && ++blk_rows == p.block_rows) {
+            if (DWM == CAKE_DWM_BLOCKED && (blk_rows += nrow) >= p.block_rows) {
                 blk_rows = 0;
 #pragma unroll
                 for (int k = 0; k < VPT; ++k)
@@ -235,10 +266,14 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) bwd_rows_kernel(const 
             st = 0;
             ph ^= 1u;
         }
-        rs_cur = rs_n1;
-        rs_n1 = rs_n2;
-        rs_n2 = rs_n3;
-        rs_n3 = rs_n4;
+#pragma unroll
+        for (int d = 0; d + 1 < kAhead; ++d)
+#pragma unroll
+            for (int i = 0; i < R2; ++i)
+                rsr[d][i] = rsr[d + 1][i];
+#pragma unroll
+        for (int i = 0; i < R2; ++i)
+            rsr[kAhead - 1][i] = rsn[i];
     }
     if (abort && lane == 0)
         set_status(p.status, kStatusTimeout);
@@ -253,7 +288,7 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) bwd_rows_kernel(const 
                 lo[k][q] = add2(lo[k][q], err);
             }
     }
-    if (!SINGLE)
+    if (FORM == kFormPair)
         pdl_launch_dependents();
 
     // ---- combine the row groups' partials in group order (shared memory)
@@ -294,7 +329,7 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) bwd_rows_kernel(const 
         }
     }
 
-    if (!SINGLE) {
+    if (FORM != kFormAtomic) {
         if (gid == 0) {
             float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);
 #pragma unroll
@@ -306,6 +341,63 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) bwd_rows_kernel(const 
                         dst[v * 4 + q] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
             }
         }
+        if (FORM == kFormPair)
+            return;
+        // ---- one-kernel fixed-order reduce: the last CTA to arrive among
+        // the kTreeGroup CTAs of its group sums their partials in CTA order
+        // into the group's total; the last group to finish sums the group
+        // totals in group order.  Nobody waits; the arithmetic order does not
+        // depend on who arrives last.
+        __threadfence();
+        consumer_sync(L);
+        const int grp = blockIdx.x / kTreeGroup;
+        const int ngroups = (gridDim.x + kTreeGroup - 1) / kTreeGroup;
+        if (threadIdx.x == 0) {
+            const int n_g = min(kTreeGroup, (int)gridDim.x - grp * kTreeGroup);
+            const unsigned prev = atomicAdd(p.tree_cnt + 1 + grp, 1u);
+            s.flag[1] = (prev == (unsigned)n_g - 1);
+        }
+        consumer_sync(L);
+        if (!s.flag[1])
+            return;
+        __threadfence();
+        const int nthr = consumer_warps * 32;
+        const int p0 = grp * kTreeGroup, p1 = min((int)gridDim.x, p0 + kTreeGroup);
+        for (int j = threadIdx.x; j < ncol; j += nthr) {
+            float2 v[kTreeGroup];
+#pragma unroll
+            for (int u = 0; u < kTreeGroup; ++u)
+                v[u] = p0 + u < p1 ? __ldcg(p.partials + (size_t)(p0 + u) * ncol + j) : make_float2(0.f, 0.f);
+            float h = 0.f, l = 0.f;
+#pragma unroll
+            for (int u = 0; u < kTreeGroup; ++u) {
+                comp_add(h, l, v[u].x);
+                l = __fadd_rn(l, v[u].y);
+            }
+            p.group_totals[(size_t)grp * ncol + j] = make_float2(h, l);
+        }
+        __threadfence();
+        consumer_sync(L);
+        if (threadIdx.x == 0) {
+            atomicExch(p.tree_cnt + 1 + grp, 0u);
+            const unsigned prev = atomicAdd(p.tree_cnt, 1u);
+            s.flag[2] = (prev == (unsigned)ngroups - 1);
+        }
+        consumer_sync(L);
+        if (!s.flag[2])
+            return;
+        __threadfence();
+        for (int j = threadIdx.x; j < ncol; j += nthr) {
+            float h = 0.f, l = 0.f;
+            for (int g2 = 0; g2 < ngroups; ++g2) {
+                const float2 v = __ldcg(p.group_totals + (size_t)g2 * ncol + j);
+                comp_add(h, l, v.x);
+                l = __fadd_rn(l, v.y);
+            }
+            p.dw[j] = __fadd_rn(h, l);
+        }
+        if (threadIdx.x == 0)
+            atomicExch(p.tree_cnt, 0u);
         return;
     }
 
@@ -406,10 +498,10 @@ __global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __gr
 
 // ------------------------------------------------------------------ launch
 
-template <int VPT, int DWM, bool SINGLE>
+template <int VPT, int DWM, int FORM, int R2>
 static cudaError_t launch_rows(const BwdParams &p, int ctas, size_t smem, cudaStream_t stream)
 {
-    auto kern = bwd_rows_kernel<VPT, DWM, SINGLE>;
+    auto kern = bwd_rows_kernel<VPT, DWM, FORM, R2>;
     cudaError_t e = ensure_smem_attr((const void *)kern, smem);
     if (e != cudaSuccess)
         return e;
@@ -418,20 +510,22 @@ static cudaError_t launch_rows(const BwdParams &p, int ctas, size_t smem, cudaSt
     return cudaGetLastError();
 }
 
-template <int VPT>
-static cudaError_t launch_vpt(const BwdParams &p, int single, int dwm, int ctas, size_t smem,
+template <int VPT, int FORM, int R2>
+static cudaError_t launch_form(const BwdParams &p, int dwm, int ctas, size_t smem, cudaStream_t stream)
+{
+    if (dwm == 0) return launch_rows<VPT, 0, FORM, R2>(p, ctas, smem, stream);
+    if (dwm == 1) return launch_rows<VPT, 1, FORM, R2>(p, ctas, smem, stream);
+    if (dwm == 2) return launch_rows<VPT, 2, FORM, R2>(p, ctas, smem, stream);
+    return launch_rows<VPT, 3, FORM, R2>(p, ctas, smem, stream);
+}
+
+template <int VPT, int R2>
+static cudaError_t launch_vpt(const BwdParams &p, int form, int dwm, int ctas, size_t smem,
                               cudaStream_t stream)
 {
-    if (single) {
-        if (dwm == 0) return launch_rows<VPT, 0, true>(p, ctas, smem, stream);
-        if (dwm == 1) return launch_rows<VPT, 1, true>(p, ctas, smem, stream);
-        if (dwm == 2) return launch_rows<VPT, 2, true>(p, ctas, smem, stream);
-        return launch_rows<VPT, 3, true>(p, ctas, smem, stream);
-    }
-    if (dwm == 0) return launch_rows<VPT, 0, false>(p, ctas, smem, stream);
-    if (dwm == 1) return launch_rows<VPT, 1, false>(p, ctas, smem, stream);
-    if (dwm == 2) return launch_rows<VPT, 2, false>(p, ctas, smem, stream);
-    return launch_rows<VPT, 3, false>(p, ctas, smem, stream);
+    if (form == kFormAtomic)
+        return launch_form<VPT, kFormAtomic, R2>(p, dwm, ctas, smem, stream);
+    return launch_form<VPT, kFormPair, R2>(p, dwm, ctas, smem, stream);
 }
 
 cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
@@ -443,11 +537,16 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
         if (e != cudaSuccess)
             return e;
     }
+    if (single == kFormTree)
+        return vpt == 1 && q.L.rows_per_group == 1 ? launch_form<1, kFormTree, 1>(q, dwm, ctas, smem, stream)
+                                                   : cudaErrorInvalidValue;
+    if (q.L.rows_per_group == 2)
+        return vpt == 1 ? launch_vpt<1, 2>(q, single, dwm, ctas, smem, stream) : cudaErrorInvalidValue;
     switch (vpt) {
-    case 1: return launch_vpt<1>(q, single, dwm, ctas, smem, stream);
-    case 2: return launch_vpt<2>(q, single, dwm, ctas, smem, stream);
-    case 3: return launch_vpt<3>(q, single, dwm, ctas, smem, stream);
-    case 4: return launch_vpt<4>(q, single, dwm, ctas, smem, stream);
+    case 1: return launch_vpt<1, 1>(q, single, dwm, ctas, smem, stream);
+    case 2: return launch_vpt<2, 1>(q, single, dwm, ctas, smem, stream);
+    case 3: return launch_vpt<3, 1>(q, single, dwm, ctas, smem, stream);
+    case 4: return launch_vpt<4, 1>(q, single, dwm, ctas, smem, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -472,38 +571,44 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int VPT, int DWM, bool SINGLE>
+template <int VPT, int DWM, int FORM, int R2>
 static cudaError_t occ_rows(int threads, size_t smem, int *n)
 {
-    auto kern = bwd_rows_kernel<VPT, DWM, SINGLE>;
+    auto kern = bwd_rows_kernel<VPT, DWM, FORM, R2>;
     cudaError_t e = ensure_smem_attr((const void *)kern, smem);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
 }
 
-template <int VPT>
-static cudaError_t occ_vpt(int single, int dwm, int threads, size_t smem, int *n)
+template <int VPT, int FORM, int R2>
+static cudaError_t occ_form(int dwm, int threads, size_t smem, int *n)
 {
-    if (single) {
-        if (dwm == 0) return occ_rows<VPT, 0, true>(threads, smem, n);
-        if (dwm == 1) return occ_rows<VPT, 1, true>(threads, smem, n);
-        if (dwm == 2) return occ_rows<VPT, 2, true>(threads, smem, n);
-        return occ_rows<VPT, 3, true>(threads, smem, n);
-    }
-    if (dwm == 0) return occ_rows<VPT, 0, false>(threads, smem, n);
-    if (dwm == 1) return occ_rows<VPT, 1, false>(threads, smem, n);
-    if (dwm == 2) return occ_rows<VPT, 2, false>(threads, smem, n);
-    return occ_rows<VPT, 3, false>(threads, smem, n);
+    if (dwm == 0) return occ_rows<VPT, 0, FORM, R2>(threads, smem, n);
+    if (dwm == 1) return occ_rows<VPT, 1, FORM, R2>(threads, smem, n);
+    if (dwm == 2) return occ_rows<VPT, 2, FORM, R2>(threads, smem, n);
+    return occ_rows<VPT, 3, FORM, R2>(threads, smem, n);
 }
 
-cudaError_t occupancy_bwd(int vpt, int single, int dwm, int threads, size_t smem, int *n)
+template <int VPT, int R2>
+static cudaError_t occ_vpt(int single, int dwm, int threads, size_t smem, int *n)
 {
+    if (single == kFormAtomic)
+        return occ_form<VPT, kFormAtomic, R2>(dwm, threads, smem, n);
+    return occ_form<VPT, kFormPair, R2>(dwm, threads, smem, n);
+}
+
+cudaError_t occupancy_bwd(int vpt, int rpg, int single, int dwm, int threads, size_t smem, int *n)
+{
+    if (single == kFormTree)
+        return vpt == 1 && rpg == 1 ? occ_form<1, kFormTree, 1>(dwm, threads, smem, n) : cudaErrorInvalidValue;
+    if (rpg == 2)
+        return vpt == 1 ? occ_vpt<1, 2>(single, dwm, threads, smem, n) : cudaErrorInvalidValue;
     switch (vpt) {
-    case 1: return occ_vpt<1>(single, dwm, threads, smem, n);
-    case 2: return occ_vpt<2>(single, dwm, threads, smem, n);
-    case 3: return occ_vpt<3>(single, dwm, threads, smem, n);
-    case 4: return occ_vpt<4>(single, dwm, threads, smem, n);
+    case 1: return occ_vpt<1, 1>(single, dwm, threads, smem, n);
+    case 2: return occ_vpt<2, 1>(single, dwm, threads, smem, n);
+    case 3: return occ_vpt<3, 1>(single, dwm, threads, smem, n);
+    case 4: return occ_vpt<4, 1>(single, dwm, threads, smem, n);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -19,6 +19,17 @@ __host__ __device__ constexpr unsigned weight_smem_bytes(int H) { return ((unsig
 // vectors per thread is compiled for; it caps the registers per thread at
 // 65536 / threads.
 __host__ __device__ constexpr int kMaxThreadsFor(int vpt) { return vpt == 1 ? 832 : 416; }
+// Largest CTA of the backward variant whose groups own two rows per stage.
+constexpr int kMaxThreadsR2 = 288;
+
+// How the backward turns the CTAs' dw partials into dw (cake_variant.single):
+// the pair (main kernel + fixed-order reduce kernel), one kernel with FP64
+// atomics, or one kernel with a fixed-order two-level reduce by the
+// last-arriving CTAs (groups of kTreeGroup CTAs).
+constexpr int kFormPair = 0;
+constexpr int kFormAtomic = 1;
+constexpr int kFormTree = 2;
+constexpr int kTreeGroup = 16;
 
 // Per-thread dw accumulation forms (same values as cake_dw_accum).
 #define CAKE_DWM_PLAIN 0
@@ -46,6 +57,7 @@ struct Layout {
     int nvec;           // H / 8: 16-byte vectors per row
     int warps_per_row;  // W
     int groups;         // NG
+    int rows_per_group; // rows a group owns per stage (1, or 2 for the backward)
     int stages;         // ring depth
     int ntens;          // tensors staged per row (x[, residual] / x, dy[, dh])
     uint32_t rows;      // total rows R = T * nh
@@ -83,6 +95,8 @@ struct BwdParams {
     float2 *partials;   // pair: [ctas][H] (hi, lo)
     double *acc;        // single: [banks][H] FP64 column accumulators (zero between calls)
     int banks;          // single: copies of the accumulators (1..16)
+    unsigned int *tree_cnt; // tree: [0] groups done, [1 + g] CTAs of group g done (zero between calls)
+    float2 *group_totals;   // tree: [ceil(P / kTreeGroup)][H] (hi, lo)
     unsigned int *arrivals; // single: CTA arrival counter (zero between calls)
     int block_rows;     // blocked accumulation: rows per FP32 block
     int *status;

@@ -27,7 +27,7 @@ constexpr int kConsumerBarrier = 9;
 struct Smem {
     uint64_t *full;   // [stages]
     uint64_t *empty;  // [stages]
-    float *red;       // [groups][2][W] (groups * W <= 25: 200 bytes)
+    float *red;       // [groups][2][R2][W] (groups * W * R2 <= 50: 400 bytes)
     int *flag;        // [4]
     float *wsm;       // [H] the weight as FP32, staged once per CTA
     uint8_t *ring;    // stages * stage_bytes
@@ -44,7 +44,7 @@ __device__ __forceinline__ Smem carve_smem(uint8_t *base, const Layout &L)
     s.flag = reinterpret_cast<int *>(base + kMiscBytes - 16);
     s.wsm = reinterpret_cast<float *>(base + kMiscBytes);
     s.ring = base + kMiscBytes + weight_smem_bytes(L.H);
-    s.tens_bytes = (uint32_t)L.groups * L.H * 2;
+    s.tens_bytes = (uint32_t)L.groups * L.rows_per_group * L.H * 2;
     s.stage_bytes = s.tens_bytes * L.ntens;
     return s;
 }
@@ -74,7 +74,7 @@ __device__ __forceinline__ Chunk cta_chunk(const Layout &L)
     c.r0 = blockIdx.x * L.rows_per_cta;
     uint32_t e = c.r0 + L.rows_per_cta;
     c.r_end = e < L.rows ? e : L.rows;
-    c.tile_rows = (uint32_t)L.groups;
+    c.tile_rows = (uint32_t)L.groups * L.rows_per_group;
     c.ntiles = c.r_end > c.r0 ? (c.r_end - c.r0 + c.tile_rows - 1) / c.tile_rows : 0;
     return c;
 }
@@ -162,6 +162,42 @@ __device__ __forceinline__ float group_sum(float v, const Smem &s, const Layout 
         red[wig] = v;
     abort = named_sync_or(1 + gid, 32 * W, abort);
     return warp_sum(lane < W ? red[lane] : 0.f);
+}
+
+// group_sum for N rows at once: the N butterflies interleave, and with
+// W > 1 one barrier serves all N rows.  Same order per row as group_sum.
+template <int N>
+__device__ __forceinline__ void group_sum_n(const float (&v)[N], float (&out)[N], const Smem &s,
+                                            const Layout &L, int gid, int wig, int lane, uint32_t slot,
+                                            bool &abort)
+{
+#pragma unroll
+    for (int n = 0; n < N; ++n)
+        out[n] = v[n];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+            out[n] += __shfl_xor_sync(0xffffffffu, out[n], o);
+    const int W = L.warps_per_row;
+    if (W == 1) {
+        abort = __any_sync(0xffffffffu, abort);
+        return;
+    }
+    float *red = s.red + (gid * 2 + (slot & 1)) * W * N;
+    if (lane == 0)
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+            red[n * W + wig] = out[n];
+    abort = named_sync_or(1 + gid, 32 * W, abort);
+#pragma unroll
+    for (int n = 0; n < N; ++n)
+        out[n] = lane < W ? red[n * W + lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+            out[n] += __shfl_xor_sync(0xffffffffu, out[n], o);
 }
 
 __device__ __forceinline__ void consumer_sync(const Layout &L)

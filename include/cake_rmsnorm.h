@@ -182,11 +182,14 @@ typedef enum {
 } cake_dw_accum;
 
 typedef struct {
-    int single;        /* 0: main + fixed-order reduce pair; 1: single kernel */
+    int single;        /* 0: main + fixed-order reduce pair; 1: single kernel,
+                          FP64 atomics; 2: single kernel, fixed-order reduce
+                          by the last-arriving CTAs (deterministic) */
     int dw_accum;      /* cake_dw_accum */
     int vec_per_thread; /* 16-byte vectors of a row held by each thread */
     int warps_per_row; /* warps that share one row */
-    int row_groups;    /* rows in flight per CTA (one per group of warps_per_row warps) */
+    int row_groups;    /* row groups (of warps_per_row warps) per CTA */
+    int rows_per_group; /* rows each group owns per pipeline stage (1 or 2) */
     int stages;        /* depth of the shared-memory ring */
     int ctas;          /* CTAs launched (P, also the number of dw partials) */
     int64_t rows_per_cta; /* contiguous rows each CTA owns */
@@ -195,9 +198,11 @@ typedef struct {
 
 /*
  * Fill *out with the variant the window table picks for this shape, weight
- * dtype, mode and residual gradient.  force_single / force_accum (-1 = let
- * the table decide) override the table, as the tests that sweep every variant
- * do; deterministic = 1 refuses force_single = 1 with CAKE_ERR_INVALID.
+ * dtype, mode and residual gradient.  force_single (0, 1 or 2 as in
+ * cake_variant.single) / force_accum (-1 = let the table decide) override
+ * the table, as the tests that sweep every variant do; deterministic = 1
+ * refuses force_single = 1 with CAKE_ERR_INVALID; force_single = 2 needs the
+ * 8-columns-per-thread layout (H <= 6144), else CAKE_ERR_UNSUPPORTED.
  */
 cake_status cake_rmsnorm_bwd_select(const cake_shape *shape, cake_dtype w_dtype,
                                     int deterministic, int has_dh, int force_single,

@@ -176,7 +176,7 @@ def test_bwd_validation(cake):
     shape = _S(300, 1, 2048)
     need = cake.cake_rmsnorm_bwd_workspace_size((300, 1, 2048))
     t = lambda: _T(A, 2048)
-    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A, need - 1) == 3      # workspace too small
+    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A, 4096) == 3          # workspace too small
     assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, None, need) == 3       # no workspace
     assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A + 16, need) == 2     # workspace not 256-B aligned
     assert _bwd(cake, shape, t(), t(), None, A, None, t(), A, A, need) == 1       # no rstd
@@ -187,3 +187,18 @@ def test_bwd_validation(cake):
     heads = _S(16, 24, 256)
     assert _bwd(cake, heads, _T(A, 24 * 256, 256), _T(A, 24 * 512, 100), A, A, None,
                 _T(A, 24 * 256, 256), A, A, 1 << 24) == 2                           # head stride not 16 B
+
+
+def test_tree_form_selection(cake):
+    v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), deterministic=True, force_single=2)
+    assert v["single"] == 2 and v["vec_per_thread"] == 1
+    v = cake.cake_rmsnorm_bwd_select((1000, 1, 2048), deterministic=False, force_single=2)
+    assert v["single"] == 2
+    with pytest.raises(cake.CakeError) as e:
+        cake.cake_rmsnorm_bwd_select((1000, 1, 8192), deterministic=True, force_single=2)
+    assert e.value.status == 2
+    # the workspace the size query reports holds every form, the tree included
+    n = cake.cake_rmsnorm_bwd_workspace_size((32768, 4, 256))
+    v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), force_single=2)
+    groups = (v["ctas"] + 15) // 16
+    assert n >= 256 + 8 * 8 * 256 + v["ctas"] * 256 * 8 + groups * 256 * 8

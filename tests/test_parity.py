@@ -143,7 +143,7 @@ def test_fwd_empty(cake):
 
 # --------------------------------------------------------------------- bwd
 
-VARIANTS = [(0, acc) for acc in (0, 1, 2, 3)] + [(1, acc) for acc in (0, 1, 2, 3)]
+VARIANTS = [(f, acc) for f in (0, 1, 2) for acc in (0, 1, 2, 3)]
 
 
 def oracle_bwd_inputs(x, w, eps, residual=None):
@@ -181,13 +181,20 @@ def check_bwd(cake, x, dy, w, eps, residual=None, dh=None, variants=VARIANTS, dw
     dx_ref_bits = None
     worst = 0.0
     for single, acc in variants:
-        det = not single
+        det = single != 1  # the pair and the one-kernel tree are deterministic
         outs = []
         for rep in range(2):
-            dx, dw = cake.cake_rmsnorm_bwd_forced(dy_d, h_d, r_d, w_d, dh_d, deterministic=det, force_single=single,
-                                                  force_accum=acc, workspace=ws)
+            try:
+                dx, dw = cake.cake_rmsnorm_bwd_forced(dy_d, h_d, r_d, w_d, dh_d, deterministic=det,
+                                                      force_single=single, force_accum=acc, workspace=ws)
+            except cake.CakeError as e:
+                # the tree form exists for the 8-columns-per-thread layout only
+                assert single == 2 and e.status == 2
+                break
             torch.cuda.synchronize()
             outs.append((bits(dx).reshape(-1, H), dw.cpu().numpy()))
+        if not outs:
+            continue
         (dxb, dwk), (dxb2, dwk2) = outs
         np.testing.assert_array_equal(dxb, dxb2)
         if det:
