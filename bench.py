@@ -207,6 +207,23 @@ def make_step_fns(cake, torch, case, dev, accum=None):
     }
 
 
+def aggregate_times(times, world, device):
+    """(max over ranks of the total ms, max over ranks of the mean ms): the
+    job takes as long as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+
+    tot = torch.tensor([sum(times), statistics.mean(times)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+    return float(tot[0]), float(tot[1])
+
+
+def replica_gbs(bytes_per_step, steps, world, slowest_total_ms):
+    """Whole-job GB/s of `world` replicas that each ran `steps` steps."""
+    return world * steps * bytes_per_step / (slowest_total_ms * 1e-3) / 1e9
+
+
 def time_loop(torch, fn, steps, warmup, flush, stream):
     """Per-step device times (ms) of fn(), the L2 flushed before every step."""
     for _ in range(warmup):
@@ -318,19 +335,14 @@ def run_ours(args):
     d2h = hdx.numel() * 2 + hdw.numel() * 4
     assert cake.cake_rmsnorm_device_status() == 0
 
-    def agg(times):
-        """(max over ranks of the total ms, max over ranks of the mean ms)."""
-        tot = torch.tensor([sum(times), statistics.mean(times)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-        return float(tot[0]), float(tot[1])
+    agg = lambda times: aggregate_times(times, world, dev)
 
     tot_det, mean_det = agg(t_det)
     tot_main, mean_main = agg(t_main)
     tot_nd, mean_nd = agg(t_nd)
     tot_fwd, mean_fwd = agg(t_fwd)
     tot_e2e, mean_e2e = agg(t_e2e)
-    gbs = lambda b, tot_ms: world * K * b / (tot_ms * 1e-3) / 1e9
+    gbs = lambda b, tot_ms: replica_gbs(b, K, world, tot_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and spec["kind"] == "plain":

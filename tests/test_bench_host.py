@@ -1,0 +1,78 @@
+"""bench.py's host-side logic without a GPU: the replica aggregation across
+ranks (world_size 2 over gloo on 127.0.0.1), the algorithmic byte counts
+and the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    times = [1.0, 2.0, 3.0] if rank == 0 else [2.0, 4.0, 6.0]  # rank 1 is the slow one
+    tot, mean = bench.aggregate_times(times, world, torch.device("cpu"))
+    out.put((rank, tot, mean))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_replica_aggregation_takes_the_slowest_rank():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for rank, tot, mean in got:
+        assert tot == 12.0 and mean == 4.0
+    sys.path.insert(0, ROOT)
+    import bench
+    # two replicas that each moved 1 GB per step, 3 steps, slowest rank 12 ms
+    assert bench.replica_gbs(1e9, 3, 2, 12.0) == pytest.approx(500.0)
+
+
+def test_workload_bytes():
+    sys.path.insert(0, ROOT)
+    import bench
+    b = bench.workload_bytes(R=65536, H=2048, w_bytes=2048 * 4, P=456)
+    assert b["rows_only"] == 6 * 65536 * 2048 + 4 * 65536 + 2048 * 4 + 4 * 2048
+    assert b["pair"] == b["rows_only"] + 2 * 8 * 456 * 2048
+    assert b["main"] == b["pair"] - 8 * 456 * 2048 - 4 * 2048
+    r = bench.workload_bytes(R=10, H=8, w_bytes=16, P=1, dh=True, res=True)
+    assert r["rows_only"] == 8 * 10 * 8 + 40 + 16 + 32
+    assert r["fwd"] == 8 * 10 * 8 + 40 + 16
+
+
+@pytest.mark.slow
+def test_reference_arm_prints_one_json_line():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+                          "--warmup", "3", "--workload", "h1536_t256"], capture_output=True, text=True, env=env,
+                         timeout=600)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
