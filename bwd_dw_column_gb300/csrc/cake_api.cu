@@ -179,18 +179,27 @@ static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int warps_per_ct
 }
 
 // Per-H CTA shape: row groups (rows in flight) per CTA and CTAs per SM.
-// About 8 consumer warps per CTA where the row allows it, then as many CTAs
+// Backward rows of several warps: one CTA per SM holding as many row groups
+// as fit its consumer warps (measured on GB300 at T = 65536: H = 1536 runs
+// 17 % faster as 4 groups in one CTA than as 3 CTAs of one group, H = 2048
+// 7 % faster as 3 groups, and the fewer CTA partials shorten the dw
+// reduction).  Otherwise about 8 consumer warps per CTA, then as many CTAs
 // per SM as the register file holds (at most 3).
 static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &groups, int &ctas_per_sm)
 {
     const int W = rl.W;
     const int max_warps = (rpg == 2 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
-    groups = W >= 8 ? 1 : 8 / W;
+    if (kind == kBwd && W > 1)
+        groups = max_warps / W > 1 ? max_warps / W : 1;
+    else
+        groups = W >= 8 ? 1 : 8 / W;
     const Tune &t = tune();
     if (t.v[kind][1] > 0)
         groups = t.v[kind][1];
     while (groups * W > max_warps && groups > 1)
         --groups;
+    if (W > 1 && groups > kMaxRowGroupBarriers) // one named barrier per group
+        groups = kMaxRowGroupBarriers;
     ctas_per_sm = resident_limit(kind, rl.vpt, rpg, dwm, groups * W + 1);
     // at most 3 resident CTAs; the forward's warp-per-row layout takes 4,
     // and its 4-warps-per-row layout runs best at 2 (GB300 measurements)
@@ -270,12 +279,12 @@ static void pick_variant(uint32_t rows, int deterministic, int &single, int &dwm
     dwm = rows <= 2048 ? CAKE_DW_PLAIN : CAKE_DW_KAHAN;
 }
 
-// Partial ranges per column per warp of the fixed-order reduce: enough CTAs
-// (about 64 or more) for small H.
+// Partial ranges per column per warp of the fixed-order reduce: about one
+// CTA per SM or more where H allows, so that each lane sums few partials.
 static int reduce_slices(int H)
 {
     int S = 1;
-    while (S < 8 && (H + 32 / S - 1) / (32 / S) < 64)
+    while (S < 8 && (H + 32 / S - 1) / (32 / S) < kSMs)
         S *= 2;
     return S;
 }

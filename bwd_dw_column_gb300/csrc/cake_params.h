@@ -21,6 +21,11 @@ __host__ __device__ constexpr unsigned weight_smem_bytes(int H) { return ((unsig
 __host__ __device__ constexpr int kMaxThreadsFor(int vpt) { return vpt == 1 ? 832 : 416; }
 // Largest CTA of the backward variant whose groups own two rows per stage.
 constexpr int kMaxThreadsR2 = 288;
+// Named barriers: 1 + g for row group g when a row spans several warps, and
+// the consumer-wide barrier after them (hardware barrier ids are 0..15).  A
+// plan whose rows span several warps has at most kMaxRowGroupBarriers groups.
+constexpr int kMaxRowGroupBarriers = 14;
+constexpr int kConsumerBarrier = kMaxRowGroupBarriers + 1;
 
 // How the backward turns the CTAs' dw partials into dw (cake_variant.single):
 // the pair (main kernel + fixed-order reduce kernel), one kernel with FP64

@@ -22,7 +22,6 @@
 namespace cake {
 
 constexpr int kStatusTimeout = 5; // == CAKE_ERR_TIMEOUT
-constexpr int kConsumerBarrier = 9;
 
 struct Smem {
     uint64_t *full;   // [stages]

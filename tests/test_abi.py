@@ -3,9 +3,11 @@ function the header declares, and its host-side logic (argument validation,
 the window table, workspace sizing) behaves as documented.  No call here
 launches a kernel."""
 import ctypes
+import json
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -187,6 +189,31 @@ def test_bwd_validation(cake):
     heads = _S(16, 24, 256)
     assert _bwd(cake, heads, _T(A, 24 * 256, 256), _T(A, 24 * 512, 100), A, A, None,
                 _T(A, 24 * 256, 256), A, A, 1 << 24) == 2                           # head stride not 16 B
+
+
+def test_row_groups_fit_named_barriers(cake):
+    # A row that spans several warps syncs on named barrier 1 + g (row group
+    # g); the consumer-wide barrier is id 15.  No plan may give a group an id
+    # of 15 or more, nor more warps than a CTA of the row kernels holds.
+    for H in range(8, 8193, 8):
+        for det in (True, False):
+            v = cake.cake_rmsnorm_bwd_select((4096, 1, H), deterministic=det)
+            if v["warps_per_row"] > 1:
+                assert v["row_groups"] <= 14
+            assert v["row_groups"] * v["warps_per_row"] * v["rows_per_group"] + 1 <= 26
+
+
+@pytest.mark.parametrize("tune", ["groups=12", "groups=24", "groups=12,cps=1"])
+def test_row_group_override_is_capped(cake, tune):
+    # the tuning override cannot push a multi-warp row past the barrier ids
+    code = ("import bwd_dw_column_gb300 as c, json; "
+            "print(json.dumps([c.cake_rmsnorm_bwd_select((65536, 1, H)) for H in (512, 1024, 1536)]))")
+    env = dict(os.environ, CAKE_TUNE=tune)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT, check=True)
+    for v in json.loads(out.stdout.strip().splitlines()[-1]):
+        assert v["warps_per_row"] > 1
+        assert v["row_groups"] <= 14
+        assert v["row_groups"] * v["warps_per_row"] + 1 <= 26
 
 
 def test_tree_form_selection(cake):
