@@ -161,10 +161,8 @@ static int kernel_regs(Kind kind, int vpt, int rpg, int dwm)
     static const int fwd[5] = {0, 48, 64, 80, 96};
     if (kind == kFwd)
         return fwd[vpt];
-    if (vpt == 1 && rpg == 2) {
-        static const int r2[4] = {104, 120, 128, 112}; // plain, blocked, twosum, kahan
-        return r2[dwm & 3];
-    }
+    if (vpt == 1 && rpg == 2)
+        return 96;
     if (vpt == 1)
         return dwm == CAKE_DW_PLAIN ? 64 : 72;
     return 128;
@@ -188,7 +186,7 @@ static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int warps_per_ct
 static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &groups, int &ctas_per_sm)
 {
     const int W = rl.W;
-    const int max_warps = (rpg == 2 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
+    const int max_warps = (rpg == 2 ? kMaxThreadsR2Wide : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
     if (kind == kBwd && W > 1)
         groups = max_warps / W > 1 ? max_warps / W : 1;
     else
@@ -216,15 +214,22 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &gro
         ctas_per_sm = t.v[kind][2];
 }
 
-// Rows a row group owns per stage: two (interleaved reductions, one barrier)
-// where the table says so, for the backward with 8 columns per thread.
+// Rows a row group owns per stage: two (interleaved, one barrier for both)
+// where a row is so wide that only one group of its warps fits a CTA (13 to
+// 19 warps: H = 3080 .. 4864), so that two rows are in flight per SM instead
+// of one (GB300, T = 65536: H = 4096 runs 14-19 % faster, H = 4608 10 %).
+// Otherwise one, and more groups per CTA instead (at 20 warps, H = 5120, two
+// rows leave 80 registers a thread: slower than one).
 static int rows_per_group(const RowLayout &rl, Kind kind)
 {
     int rpg = 1;
+    const int one_row_groups = (kMaxThreadsFor(rl.vpt) / 32 - 1) / rl.W;
+    if (kind == kBwd && rl.W > 1 && one_row_groups < 2)
+        rpg = 2;
     const int forced = tune().v[kind][4];
     if (forced == 1 || forced == 2)
         rpg = forced;
-    if (kind != kBwd || rl.vpt != 1 || rl.W > 8)
+    if (kind != kBwd || rl.vpt != 1 || rl.W > kMaxThreadsR2Wide / 32 - 1)
         rpg = 1;
     return rpg;
 }

@@ -59,8 +59,7 @@ static cudaError_t status_ptr(int **out)
 }
 
 template <int VPT, int DWM, int FORM, int R2>
-__global__ void __launch_bounds__(R2 == 1 ? kMaxThreadsFor(VPT) : kMaxThreadsR2, 1)
-    bwd_rows_kernel(const __grid_constant__ BwdParams p)
+__device__ __forceinline__ void bwd_rows(const BwdParams &p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const Layout &L = p.L;
@@ -440,6 +439,17 @@ __global__ void __launch_bounds__(R2 == 1 ? kMaxThreadsFor(VPT) : kMaxThreadsR2,
     }
 }
 
+// The row kernels: one row per group, or two (R2 = 2: one group of up to 16
+// warps and the producer per CTA; R2 = 3: the same code built for up to 19
+// warps).  The bounds cap the registers a thread may use so that the largest
+// CTA fits: 72 (26 warps), 96 (17 or 20 warps), 128 (13 warps).
+template <int VPT, int DWM, int FORM, int R2>
+__global__ void __launch_bounds__(R2 == 1 ? kMaxThreadsFor(VPT) : R2 == 2 ? kMaxThreadsR2 : kMaxThreadsR2Wide, 1)
+    bwd_rows_kernel(const __grid_constant__ BwdParams p)
+{
+    bwd_rows<VPT, DWM, FORM, R2 == 1 ? 1 : 2>(p);
+}
+
 // Fixed-order reduction of the pair's CTA partials.  A CTA owns C columns
 // (C = 32 / S) and 16 warps; lane = (slice s, column c).  The P partials of a
 // column are split into 16*S contiguous ranges in ascending order, range
@@ -501,12 +511,15 @@ __global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __gr
 template <int VPT, int DWM, int FORM, int R2>
 static cudaError_t launch_rows(const BwdParams &p, int ctas, size_t smem, cudaStream_t stream)
 {
-    auto kern = bwd_rows_kernel<VPT, DWM, FORM, R2>;
-    cudaError_t e = ensure_smem_attr((const void *)kern, smem);
+    const int threads = 32 * (p.L.groups * p.L.warps_per_row + 1);
+    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, R2>;
+    cudaError_t e = ensure_smem_attr(kern, smem);
     if (e != cudaSuccess)
         return e;
-    const int threads = 32 * (p.L.groups * p.L.warps_per_row + 1);
-    kern<<<ctas, threads, smem, stream>>>(p);
+    void *args[] = {const_cast<BwdParams *>(&p)};
+    e = cudaLaunchKernel(kern, dim3((unsigned)ctas), dim3((unsigned)threads), args, smem, stream);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
@@ -540,8 +553,12 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
     if (single == kFormTree)
         return vpt == 1 && q.L.rows_per_group == 1 ? launch_form<1, kFormTree, 1>(q, dwm, ctas, smem, stream)
                                                    : cudaErrorInvalidValue;
-    if (q.L.rows_per_group == 2)
-        return vpt == 1 ? launch_vpt<1, 2>(q, single, dwm, ctas, smem, stream) : cudaErrorInvalidValue;
+    if (q.L.rows_per_group == 2) {
+        if (vpt != 1)
+            return cudaErrorInvalidValue;
+        return q.L.warps_per_row + 1 <= kMaxThreadsR2 / 32 ? launch_vpt<1, 2>(q, single, dwm, ctas, smem, stream)
+                                                           : launch_vpt<1, 3>(q, single, dwm, ctas, smem, stream);
+    }
     switch (vpt) {
     case 1: return launch_vpt<1, 1>(q, single, dwm, ctas, smem, stream);
     case 2: return launch_vpt<2, 1>(q, single, dwm, ctas, smem, stream);
@@ -574,8 +591,8 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
 template <int VPT, int DWM, int FORM, int R2>
 static cudaError_t occ_rows(int threads, size_t smem, int *n)
 {
-    auto kern = bwd_rows_kernel<VPT, DWM, FORM, R2>;
-    cudaError_t e = ensure_smem_attr((const void *)kern, smem);
+    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, R2>;
+    cudaError_t e = ensure_smem_attr(kern, smem);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
@@ -602,8 +619,12 @@ cudaError_t occupancy_bwd(int vpt, int rpg, int single, int dwm, int threads, si
 {
     if (single == kFormTree)
         return vpt == 1 && rpg == 1 ? occ_form<1, kFormTree, 1>(dwm, threads, smem, n) : cudaErrorInvalidValue;
-    if (rpg == 2)
-        return vpt == 1 ? occ_vpt<1, 2>(single, dwm, threads, smem, n) : cudaErrorInvalidValue;
+    if (rpg == 2) {
+        if (vpt != 1)
+            return cudaErrorInvalidValue;
+        return threads <= kMaxThreadsR2 ? occ_vpt<1, 2>(single, dwm, threads, smem, n)
+                                        : occ_vpt<1, 3>(single, dwm, threads, smem, n);
+    }
     switch (vpt) {
     case 1: return occ_vpt<1, 1>(single, dwm, threads, smem, n);
     case 2: return occ_vpt<2, 1>(single, dwm, threads, smem, n);
