@@ -186,7 +186,7 @@ static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int warps_per_ct
 static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &groups, int &ctas_per_sm)
 {
     const int W = rl.W;
-    const int max_warps = (rpg == 2 ? kMaxThreadsR2Wide : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
+    const int max_warps = (rpg == 2 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
     if (kind == kBwd && W > 1)
         groups = max_warps / W > 1 ? max_warps / W : 1;
     else
@@ -216,10 +216,9 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &gro
 
 // Rows a row group owns per stage: two (interleaved, one barrier for both)
 // where a row is so wide that only one group of its warps fits a CTA (13 to
-// 19 warps: H = 3080 .. 4864), so that two rows are in flight per SM instead
-// of one (GB300, T = 65536: H = 4096 runs 14-19 % faster, H = 4608 10 %).
-// Otherwise one, and more groups per CTA instead (at 20 warps, H = 5120, two
-// rows leave 80 registers a thread: slower than one).
+// 20 warps: H = 3080 .. 5120), so that two rows are in flight per SM instead
+// of one (GB300, T = 65536: H = 3584 det 16 % faster, H = 4096 19 %, H =
+// 4608 10 %, H = 5120 6 %).  Otherwise one, and more groups per CTA.
 static int rows_per_group(const RowLayout &rl, Kind kind)
 {
     int rpg = 1;
@@ -229,7 +228,7 @@ static int rows_per_group(const RowLayout &rl, Kind kind)
     const int forced = tune().v[kind][4];
     if (forced == 1 || forced == 2)
         rpg = forced;
-    if (kind != kBwd || rl.vpt != 1 || rl.W > kMaxThreadsR2Wide / 32 - 1)
+    if (kind != kBwd || rl.vpt != 1 || rl.W > kMaxThreadsR2 / 32 - 1)
         rpg = 1;
     return rpg;
 }

@@ -58,7 +58,7 @@ static cudaError_t status_ptr(int **out)
     return cudaSuccess;
 }
 
-template <int VPT, int DWM, int FORM, int R2>
+template <int VPT, int DWM, int FORM, int R2, bool KEEP>
 __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -134,7 +134,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             // terms dy*h*rstd (dy*h is exact in FP32), rows in order.
             // VPT == 1 keeps x and m in registers for the dx step; wider
             // layouts re-read the staged row instead (fewer registers).
-            constexpr bool kKeep = VPT == 1;
+            constexpr bool kKeep = VPT == 1 && KEEP;
             float2 x2[R2][kKeep ? VPT : 1][4], m2[R2][kKeep ? VPT : 1][4];
             float dot[R2];
 #pragma unroll
@@ -439,15 +439,25 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     }
 }
 
-// The row kernels: one row per group, or two (R2 = 2: one group of up to 16
-// warps and the producer per CTA; R2 = 3: the same code built for up to 19
-// warps).  The bounds cap the registers a thread may use so that the largest
-// CTA fits: 72 (26 warps), 96 (17 or 20 warps), 128 (13 warps).
-template <int VPT, int DWM, int FORM, int R2>
-__global__ void __launch_bounds__(R2 == 1 ? kMaxThreadsFor(VPT) : R2 == 2 ? kMaxThreadsR2 : kMaxThreadsR2Wide, 1)
+// The row kernels, by row build RB: 0 one row per group; two rows per group
+// (one group and the producer per CTA) keeping x and dy*w in registers for
+// CTAs of up to 17 (1) or 20 (2) warps, or re-reading them for 21 warps (3).
+// The bounds cap the registers a thread may use so that the largest CTA
+// fits: 72 (26 warps), 96 (17 or 20 warps), 80 (21 warps), 128 (13 warps).
+template <int VPT, int DWM, int FORM, int RB>
+__global__ void __launch_bounds__(RB == 0 ? kMaxThreadsFor(VPT) : kRowBuildThreads[RB], 1)
     bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
-    bwd_rows<VPT, DWM, FORM, R2 == 1 ? 1 : 2>(p);
+    bwd_rows<VPT, DWM, FORM, RB == 0 ? 1 : 2, RB != 3>(p);
+}
+
+// Row build of a two-rows-per-group CTA of `threads` threads.
+static int two_row_build(int threads)
+{
+    for (int rb = 1; rb <= 3; ++rb)
+        if (threads <= kRowBuildThreads[rb])
+            return rb;
+    return 0;
 }
 
 // Fixed-order reduction of the pair's CTA partials.  A CTA owns C columns
@@ -508,11 +518,11 @@ __global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __gr
 
 // ------------------------------------------------------------------ launch
 
-template <int VPT, int DWM, int FORM, int R2>
+template <int VPT, int DWM, int FORM, int RB>
 static cudaError_t launch_rows(const BwdParams &p, int ctas, size_t smem, cudaStream_t stream)
 {
     const int threads = 32 * (p.L.groups * p.L.warps_per_row + 1);
-    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, R2>;
+    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, RB>;
     cudaError_t e = ensure_smem_attr(kern, smem);
     if (e != cudaSuccess)
         return e;
@@ -523,22 +533,22 @@ static cudaError_t launch_rows(const BwdParams &p, int ctas, size_t smem, cudaSt
     return cudaGetLastError();
 }
 
-template <int VPT, int FORM, int R2>
+template <int VPT, int FORM, int RB>
 static cudaError_t launch_form(const BwdParams &p, int dwm, int ctas, size_t smem, cudaStream_t stream)
 {
-    if (dwm == 0) return launch_rows<VPT, 0, FORM, R2>(p, ctas, smem, stream);
-    if (dwm == 1) return launch_rows<VPT, 1, FORM, R2>(p, ctas, smem, stream);
-    if (dwm == 2) return launch_rows<VPT, 2, FORM, R2>(p, ctas, smem, stream);
-    return launch_rows<VPT, 3, FORM, R2>(p, ctas, smem, stream);
+    if (dwm == 0) return launch_rows<VPT, 0, FORM, RB>(p, ctas, smem, stream);
+    if (dwm == 1) return launch_rows<VPT, 1, FORM, RB>(p, ctas, smem, stream);
+    if (dwm == 2) return launch_rows<VPT, 2, FORM, RB>(p, ctas, smem, stream);
+    return launch_rows<VPT, 3, FORM, RB>(p, ctas, smem, stream);
 }
 
-template <int VPT, int R2>
+template <int VPT, int RB>
 static cudaError_t launch_vpt(const BwdParams &p, int form, int dwm, int ctas, size_t smem,
                               cudaStream_t stream)
 {
     if (form == kFormAtomic)
-        return launch_form<VPT, kFormAtomic, R2>(p, dwm, ctas, smem, stream);
-    return launch_form<VPT, kFormPair, R2>(p, dwm, ctas, smem, stream);
+        return launch_form<VPT, kFormAtomic, RB>(p, dwm, ctas, smem, stream);
+    return launch_form<VPT, kFormPair, RB>(p, dwm, ctas, smem, stream);
 }
 
 cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
@@ -551,19 +561,23 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
             return e;
     }
     if (single == kFormTree)
-        return vpt == 1 && q.L.rows_per_group == 1 ? launch_form<1, kFormTree, 1>(q, dwm, ctas, smem, stream)
+        return vpt == 1 && q.L.rows_per_group == 1 ? launch_form<1, kFormTree, 0>(q, dwm, ctas, smem, stream)
                                                    : cudaErrorInvalidValue;
     if (q.L.rows_per_group == 2) {
         if (vpt != 1)
             return cudaErrorInvalidValue;
-        return q.L.warps_per_row + 1 <= kMaxThreadsR2 / 32 ? launch_vpt<1, 2>(q, single, dwm, ctas, smem, stream)
-                                                           : launch_vpt<1, 3>(q, single, dwm, ctas, smem, stream);
+        switch (two_row_build(32 * (q.L.groups * q.L.warps_per_row + 1))) {
+        case 1: return launch_vpt<1, 1>(q, single, dwm, ctas, smem, stream);
+        case 2: return launch_vpt<1, 2>(q, single, dwm, ctas, smem, stream);
+        case 3: return launch_vpt<1, 3>(q, single, dwm, ctas, smem, stream);
+        default: return cudaErrorInvalidValue;
+        }
     }
     switch (vpt) {
-    case 1: return launch_vpt<1, 1>(q, single, dwm, ctas, smem, stream);
-    case 2: return launch_vpt<2, 1>(q, single, dwm, ctas, smem, stream);
-    case 3: return launch_vpt<3, 1>(q, single, dwm, ctas, smem, stream);
-    case 4: return launch_vpt<4, 1>(q, single, dwm, ctas, smem, stream);
+    case 1: return launch_vpt<1, 0>(q, single, dwm, ctas, smem, stream);
+    case 2: return launch_vpt<2, 0>(q, single, dwm, ctas, smem, stream);
+    case 3: return launch_vpt<3, 0>(q, single, dwm, ctas, smem, stream);
+    case 4: return launch_vpt<4, 0>(q, single, dwm, ctas, smem, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -588,48 +602,52 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int VPT, int DWM, int FORM, int R2>
+template <int VPT, int DWM, int FORM, int RB>
 static cudaError_t occ_rows(int threads, size_t smem, int *n)
 {
-    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, R2>;
+    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, RB>;
     cudaError_t e = ensure_smem_attr(kern, smem);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
 }
 
-template <int VPT, int FORM, int R2>
+template <int VPT, int FORM, int RB>
 static cudaError_t occ_form(int dwm, int threads, size_t smem, int *n)
 {
-    if (dwm == 0) return occ_rows<VPT, 0, FORM, R2>(threads, smem, n);
-    if (dwm == 1) return occ_rows<VPT, 1, FORM, R2>(threads, smem, n);
-    if (dwm == 2) return occ_rows<VPT, 2, FORM, R2>(threads, smem, n);
-    return occ_rows<VPT, 3, FORM, R2>(threads, smem, n);
+    if (dwm == 0) return occ_rows<VPT, 0, FORM, RB>(threads, smem, n);
+    if (dwm == 1) return occ_rows<VPT, 1, FORM, RB>(threads, smem, n);
+    if (dwm == 2) return occ_rows<VPT, 2, FORM, RB>(threads, smem, n);
+    return occ_rows<VPT, 3, FORM, RB>(threads, smem, n);
 }
 
-template <int VPT, int R2>
+template <int VPT, int RB>
 static cudaError_t occ_vpt(int single, int dwm, int threads, size_t smem, int *n)
 {
     if (single == kFormAtomic)
-        return occ_form<VPT, kFormAtomic, R2>(dwm, threads, smem, n);
-    return occ_form<VPT, kFormPair, R2>(dwm, threads, smem, n);
+        return occ_form<VPT, kFormAtomic, RB>(dwm, threads, smem, n);
+    return occ_form<VPT, kFormPair, RB>(dwm, threads, smem, n);
 }
 
 cudaError_t occupancy_bwd(int vpt, int rpg, int single, int dwm, int threads, size_t smem, int *n)
 {
     if (single == kFormTree)
-        return vpt == 1 && rpg == 1 ? occ_form<1, kFormTree, 1>(dwm, threads, smem, n) : cudaErrorInvalidValue;
+        return vpt == 1 && rpg == 1 ? occ_form<1, kFormTree, 0>(dwm, threads, smem, n) : cudaErrorInvalidValue;
     if (rpg == 2) {
         if (vpt != 1)
             return cudaErrorInvalidValue;
-        return threads <= kMaxThreadsR2 ? occ_vpt<1, 2>(single, dwm, threads, smem, n)
-                                        : occ_vpt<1, 3>(single, dwm, threads, smem, n);
+        switch (two_row_build(threads)) {
+        case 1: return occ_vpt<1, 1>(single, dwm, threads, smem, n);
+        case 2: return occ_vpt<1, 2>(single, dwm, threads, smem, n);
+        case 3: return occ_vpt<1, 3>(single, dwm, threads, smem, n);
+        default: return cudaErrorInvalidValue;
+        }
     }
     switch (vpt) {
-    case 1: return occ_vpt<1, 1>(single, dwm, threads, smem, n);
-    case 2: return occ_vpt<2, 1>(single, dwm, threads, smem, n);
-    case 3: return occ_vpt<3, 1>(single, dwm, threads, smem, n);
-    case 4: return occ_vpt<4, 1>(single, dwm, threads, smem, n);
+    case 1: return occ_vpt<1, 0>(single, dwm, threads, smem, n);
+    case 2: return occ_vpt<2, 0>(single, dwm, threads, smem, n);
+    case 3: return occ_vpt<3, 0>(single, dwm, threads, smem, n);
+    case 4: return occ_vpt<4, 0>(single, dwm, threads, smem, n);
     default: return cudaErrorInvalidValue;
     }
 }

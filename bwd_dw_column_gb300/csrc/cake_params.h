@@ -19,14 +19,14 @@ __host__ __device__ constexpr unsigned weight_smem_bytes(int H) { return ((unsig
 // vectors per thread is compiled for; it caps the registers per thread at
 // 65536 / threads.
 __host__ __device__ constexpr int kMaxThreadsFor(int vpt) { return vpt == 1 ? 832 : 416; }
-// Largest CTAs of the backward variant whose groups own two rows per stage
-// (one group and the producer): up to 16 warps, and a wider build for 17 to
-// 19.  A CTA's warps spread over the SM's four register files of 16384: 20
-// warps (5 per file) leave 96 registers a thread, 21 warps only 80.  Both
-// builds use 96 registers; the narrower bound schedules better (GB300, H =
-// 4096: 6 % faster).
-constexpr int kMaxThreadsR2 = 544;
-constexpr int kMaxThreadsR2Wide = 640;
+// Largest CTAs of the backward builds whose groups own two rows per stage
+// (one group and the producer), by row build 1..3 (index 0 unused).  A CTA's
+// warps spread over the SM's four register files of 16384: 17 to 20 warps
+// (5 per file) leave 96 registers a thread, 21 warps (6) only 80 -- too few
+// to keep x and dy*w of two rows in registers, so build 3 re-reads them.  The
+// 17-warp bound schedules better than the 20-warp one (GB300, H = 4096: 6 %).
+constexpr int kRowBuildThreads[4] = {0, 544, 640, 672};
+constexpr int kMaxThreadsR2 = 672;
 // Named barriers: 1 + g for row group g when a row spans several warps, and
 // the consumer-wide barrier after them (hardware barrier ids are 0..15).  A
 // plan whose rows span several warps has at most kMaxRowGroupBarriers groups.
