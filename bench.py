@@ -198,10 +198,16 @@ def make_step_fns(cake, torch, case, dev, accum=None):
         return lambda: cake.cake_rmsnorm_bwd_forced(dy, h, rstd, w, dh, deterministic=det, force_single=int(not det),
                                                    force_accum=accum, workspace=ws, dx=dx, dw=dw)
 
+    def forced(form):
+        return lambda: cake.cake_rmsnorm_bwd_forced(dy, h, rstd, w, dh, deterministic=form != 1, force_single=form,
+                                                   force_accum=accum, workspace=ws, dx=dx, dw=dw)
+
     return {
         "fwd": lambda: cake.cake_rmsnorm_fwd(x, w, eps, residual=res, y=y, rstd=rstd, h_new=hn),
         "det": bwd(True),
         "nondet": bwd(False),
+        "single_atomic": forced(1),
+        "single_grid": forced(3),
         "main": lambda: cake.cake_rmsnorm_bwd_main(dy, h, rstd, w, dh, workspace=ws, dx=dx, dw=dw, force_accum=accum),
         "h": h, "rstd": rstd, "ws": ws, "dx": dx, "dw": dw,
     }
@@ -323,6 +329,8 @@ def run_ours(args):
         t_det = time_loop(torch, fns["det"], K, Wm, flush, stream)
         t_main = time_loop(torch, fns["main"], K, Wm, flush, stream)
         t_nd = time_loop(torch, fns["nondet"], K, Wm, flush, stream)
+        t_sa = time_loop(torch, fns["single_atomic"], K, Wm, flush, stream)
+        t_sg = time_loop(torch, fns["single_grid"], K, Wm, flush, stream)
         t_fwd = time_loop(torch, fns["fwd"], K, Wm, flush, stream)
     torch.cuda.synchronize()
     clocks = clk.summary()
@@ -365,6 +373,9 @@ def run_ours(args):
     tot_det, mean_det = agg(t_det)
     tot_main, mean_main = agg(t_main)
     tot_nd, mean_nd = agg(t_nd)
+    tot_sa, mean_sa = agg(t_sa)
+    tot_sg, mean_sg = agg(t_sg)
+    nd_bytes = nbytes["pair"] if nd_variant["single"] == 0 else nbytes["single"]
     tot_fwd, mean_fwd = agg(t_fwd)
     tot_e2e, mean_e2e = agg(t_e2e)
     gbs = lambda b, tot_ms: replica_gbs(b, K, world, tot_ms)
@@ -414,8 +425,15 @@ def run_ours(args):
                          "bytes": nbytes["pair"]},
             "det_main_kernel": {"us": round(mean_main * 1e3, 2), "GB/s": round(achieved_main, 1),
                                 "bytes": nbytes["main"]},
-            "nondet": {"us": round(mean_nd * 1e3, 2), "GB/s": round(gbs(nbytes["single"], tot_nd), 1),
-                       "bytes": nbytes["single"], "variant": nd_variant},
+            "nondet": {"us": round(mean_nd * 1e3, 2), "GB/s": round(gbs(nd_bytes, tot_nd), 1),
+                       "bytes": nd_bytes, "variant": nd_variant},
+            # the single-kernel forms the non-deterministic mode may run
+            # (the table picks the pair, which is faster at every measured
+            # shape): FP64 L2 atomics, and the cooperative grid form
+            "single_atomic": {"us": round(mean_sa * 1e3, 2), "GB/s": round(gbs(nbytes["single"], tot_sa), 1),
+                              "bytes": nbytes["single"]},
+            "single_grid": {"us": round(mean_sg * 1e3, 2), "GB/s": round(gbs(nbytes["pair"], tot_sg), 1),
+                            "bytes": nbytes["pair"]},
             "fwd": {"us": round(mean_fwd * 1e3, 2), "GB/s": round(gbs(nbytes["fwd"], tot_fwd), 1),
                     "bytes": nbytes["fwd"]},
         },
@@ -437,9 +455,9 @@ def run_ours(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
         },
-        "gpu_launches": K * (2 + 1 + (1 if nd_variant["single"] else 2) + 1 + 2),
+        "gpu_launches": K * (2 + 1 + (1 if nd_variant["single"] else 2) + 1 + 1 + 1 + 2),
         "gpu_launches_detail": {"det": 2 * K, "main_only": K, "nondet": K * (1 if nd_variant["single"] else 2),
-                                "fwd": K, "e2e": 2 * K},
+                                "single_atomic": K, "single_grid": K, "fwd": K, "e2e": 2 * K},
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

@@ -271,15 +271,23 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     return p;
 }
 
-// Mode / accumulation choice.  Deterministic: the pair.  Non-deterministic:
-// the single kernel (FP64 column accumulation in L2).  Per-thread
-// accumulation: up to 2048 rows the plain FP32 sum (a thread sums a handful
-// of rows, far inside the budget); above, Kahan's compensated sum of the
-// rounded products, which leaves only the products' own rounding and costs
-// about as much as the blocked form.
+// Mode / accumulation choice.  Deterministic: the pair.  Non-deterministic
+// mode may run a single kernel -- FP64 column accumulation in L2 (1), the
+// tree (2) or the cooperative grid form (3) -- but the table picks one only
+// where it beats the pair, and on GB300 none does at any measured shape: the
+// pair's reduce, launched as a programmatic dependent of the main kernel,
+// adds 2-5 us after it, while the single kernels' tails (the last CTA's
+// finalise behind the L2 atomics, or the grid barrier) add 4-27 us (T =
+// 32768 .. 131072, H = 256 .. 6144).  So both modes run the pair, whose dw
+// is also reproducible; CAKE_TUNE=form=N or force_single selects a single
+// kernel.  Per-thread accumulation: up to 2048 rows the plain FP32 sum (a
+// thread sums a handful of rows, far inside the budget); above, Kahan's
+// compensated sum of the rounded products, which leaves only the products'
+// own rounding and costs about as much as the blocked form.
 static void pick_variant(uint32_t rows, int deterministic, int &single, int &dwm)
 {
-    single = deterministic ? 0 : 1;
+    (void)deterministic;
+    single = kFormPair;
     dwm = rows <= 2048 ? CAKE_DW_PLAIN : CAKE_DW_KAHAN;
 }
 
@@ -295,7 +303,12 @@ static int reduce_slices(int H)
 
 // ---------------------------------------------------------- workspace layout
 
-constexpr size_t kWsHeader = 256; // arrival counter (+ padding)
+// Header words (u32): [0] the single kernel's arrival counter; [1 .. 1 + 1 +
+// kTreeMaxGroups] the tree form's counters; [kGridWords, +1] the grid form's
+// barrier counter and generation.
+constexpr size_t kWsHeader = 512;
+constexpr int kTreeMaxGroups = 62;
+constexpr int kGridWords = 64;
 constexpr int kAccBanks = 8;      // copies of the single kernel's FP64 accumulators
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -426,7 +439,7 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
     cake_status st = check_shape(shape, rows);
     if (st != CAKE_OK)
         return st;
-    if (force_single > kFormTree || force_accum > CAKE_DW_KAHAN)
+    if (force_single > kFormGrid || force_accum > CAKE_DW_KAHAN)
         return CAKE_ERR_INVALID;
     if (deterministic && force_single == kFormAtomic)
         return CAKE_ERR_INVALID;
@@ -440,7 +453,7 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
         dwm = force_accum;
     *plan = make_plan((int)shape->hidden, *rows, has_dh ? 3 : 2, kBwd, single, dwm);
     if (plan->single == kFormTree &&
-        (plan->rl.vpt != 1 || plan->rpg != 1 || tree_groups(plan->ctas) > (int)(kWsHeader / 4) - 2))
+        (plan->rl.vpt != 1 || plan->rpg != 1 || tree_groups(plan->ctas) > kTreeMaxGroups))
         return CAKE_ERR_UNSUPPORTED;
     return CAKE_OK;
 }
@@ -505,6 +518,8 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.partials = reinterpret_cast<float2 *>(ws + ws_part_off(H));
     p.tree_cnt = reinterpret_cast<unsigned int *>(ws) + 1;
     p.group_totals = reinterpret_cast<float2 *>(ws + ws_tree_off(H, plan.ctas));
+    p.grid_cnt = reinterpret_cast<unsigned int *>(ws) + kGridWords;
+    p.grid_gen = reinterpret_cast<unsigned int *>(ws) + kGridWords + 1;
     // the accumulator banks that fit the given workspace (the built-in
     // scratch of the allocation-free entry point may hold fewer than 8)
     {
@@ -532,7 +547,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
 // and its FP64 column accumulators -- lives in this library-owned array
 // instead of a workspace.  It is loaded with the library and stays resident
 // on every GPU that uses the library until the process exits.
-constexpr size_t kNoAllocScratchBytes = 256 + 8 * (size_t)CAKE_NOALLOC_MAX_HIDDEN;
+constexpr size_t kNoAllocScratchBytes = kWsHeader + 8 * (size_t)CAKE_NOALLOC_MAX_HIDDEN;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {

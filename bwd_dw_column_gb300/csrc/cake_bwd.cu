@@ -342,6 +342,48 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         }
         if (FORM == kFormPair)
             return;
+        if (FORM == kFormGrid) {
+            // ---- cooperative form: every CTA's partial is written; after
+            // the grid barrier CTA b reduces columns [b*C, (b+1)*C), one
+            // column per warp at a time: lane l sums the partials of CTAs
+            // [l*per, (l+1)*per) in ascending order (compensated), then the
+            // 32 lane sums merge in a butterfly whose every step is
+            // symmetric, so the result is the same on every lane and run.
+            consumer_sync(L);
+            if (threadIdx.x == 0)
+                s.flag[1] = grid_barrier(p.grid_cnt, p.grid_gen, gridDim.x);
+            consumer_sync(L);
+            if (!s.flag[1]) {
+                if (threadIdx.x == 0)
+                    set_status(p.status, kStatusTimeout);
+                return;
+            }
+            const int P = (int)gridDim.x;
+            const int C = (ncol + P - 1) / P;
+            const int c0 = (int)blockIdx.x * C, c1 = min(ncol, c0 + C);
+            const int per = (P + 31) / 32;
+            const int q0 = lane * per, q1 = min(P, q0 + per);
+            for (int j = c0 + warp; j < c1; j += consumer_warps) {
+                float h = 0.f, l = 0.f;
+                for (int q = q0; q < q1; q += 4) {
+                    float2 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        v[u] = q + u < q1 ? __ldcg(p.partials + (size_t)(q + u) * ncol + j) : make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        comp_add(h, l, v[u].x);
+                        l = __fadd_rn(l, v[u].y);
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1)
+                    comp_merge(h, l, __shfl_xor_sync(0xffffffffu, h, o), __shfl_xor_sync(0xffffffffu, l, o));
+                if (lane == 0)
+                    p.dw[j] = __fadd_rn(h, l);
+            }
+            return;
+        }
         // ---- one-kernel fixed-order reduce: the last CTA to arrive among
         // the kTreeGroup CTAs of its group sums their partials in CTA order
         // into the group's total; the last group to finish sums the group
@@ -522,12 +564,23 @@ template <int VPT, int DWM, int FORM, int RB>
 static cudaError_t launch_rows(const BwdParams &p, int ctas, size_t smem, cudaStream_t stream)
 {
     const int threads = 32 * (p.L.groups * p.L.warps_per_row + 1);
-    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, RB>;
-    cudaError_t e = ensure_smem_attr(kern, smem);
+    auto kern = bwd_rows_kernel<VPT, DWM, FORM, RB>;
+    cudaError_t e = ensure_smem_attr((const void *)kern, smem);
     if (e != cudaSuccess)
         return e;
-    void *args[] = {const_cast<BwdParams *>(&p)};
-    e = cudaLaunchKernel(kern, dim3((unsigned)ctas), dim3((unsigned)threads), args, smem, stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    // the grid form's CTAs wait for one another: the launch must guarantee
+    // that they are all resident at once (it fails otherwise)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = FORM == kFormGrid ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -548,6 +601,8 @@ static cudaError_t launch_vpt(const BwdParams &p, int form, int dwm, int ctas, s
 {
     if (form == kFormAtomic)
         return launch_form<VPT, kFormAtomic, RB>(p, dwm, ctas, smem, stream);
+    if (form == kFormGrid)
+        return launch_form<VPT, kFormGrid, RB>(p, dwm, ctas, smem, stream);
     return launch_form<VPT, kFormPair, RB>(p, dwm, ctas, smem, stream);
 }
 
@@ -626,6 +681,8 @@ static cudaError_t occ_vpt(int single, int dwm, int threads, size_t smem, int *n
 {
     if (single == kFormAtomic)
         return occ_form<VPT, kFormAtomic, RB>(dwm, threads, smem, n);
+    if (single == kFormGrid)
+        return occ_form<VPT, kFormGrid, RB>(dwm, threads, smem, n);
     return occ_form<VPT, kFormPair, RB>(dwm, threads, smem, n);
 }
 

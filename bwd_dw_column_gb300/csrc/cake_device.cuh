@@ -208,6 +208,58 @@ __device__ __forceinline__ void comp_add(float &hi, float &lo, float v)
 
 // --------------------------------------------------------- row addressing
 
+// GPU-scope loads for a flag other CTAs publish.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier of one thread per CTA (all CTAs co-resident: a
+// cooperative launch).  cnt counts arrivals; the last CTA to arrive resets
+// it and advances gen, which the others wait on.  Before it the caller's
+// CTA has synchronised, so the fence + add publishes the whole CTA's writes
+// (a release; the acquire loads / fence make the other CTAs' writes visible
+// to this CTA after its next barrier).  Returns false if gen has not moved
+// within kWaitLimitNs.
+__device__ __forceinline__ bool grid_barrier(uint32_t *cnt, uint32_t *gen, uint32_t nctas)
+{
+    const uint32_t g0 = ld_relaxed_gpu(gen);
+    __threadfence();
+    if (atomicAdd(cnt, 1u) == nctas - 1) {
+        atomicExch(cnt, 0u);
+        __threadfence();
+        atomicAdd(gen, 1u);
+        return true;
+    }
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ld_acquire_gpu(gen) != g0)
+            return true;
+        __nanosleep(64);
+        if ((i & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+// (h, l) + (h2, l2) as a compensated pair, symmetric in its two operands
+// (the result does not depend on their order).
+__device__ __forceinline__ void comp_merge(float &h, float &l, float h2, float l2)
+{
+    float s, e;
+    two_sum(h, h2, s, e);
+    l = __fadd_rn(__fadd_rn(l, l2), e);
+    h = s;
+}
+
 // Element offset of row r in a [T, nh, H] view.
 __device__ __forceinline__ int64_t row_off(const RowView &v, uint32_t r, uint32_t nh)
 {

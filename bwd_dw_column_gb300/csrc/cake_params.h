@@ -35,11 +35,14 @@ constexpr int kConsumerBarrier = kMaxRowGroupBarriers + 1;
 
 // How the backward turns the CTAs' dw partials into dw (cake_variant.single):
 // the pair (main kernel + fixed-order reduce kernel), one kernel with FP64
-// atomics, or one kernel with a fixed-order two-level reduce by the
-// last-arriving CTAs (groups of kTreeGroup CTAs).
+// atomics, one kernel with a fixed-order two-level reduce by the
+// last-arriving CTAs (groups of kTreeGroup CTAs), or one cooperative kernel
+// whose CTAs meet at a grid barrier and then each reduce a slice of the
+// columns in fixed order.
 constexpr int kFormPair = 0;
 constexpr int kFormAtomic = 1;
 constexpr int kFormTree = 2;
+constexpr int kFormGrid = 3;
 constexpr int kTreeGroup = 16;
 
 // Per-thread dw accumulation forms (same values as cake_dw_accum).
@@ -108,6 +111,8 @@ struct BwdParams {
     int banks;          // single: copies of the accumulators (1..16)
     unsigned int *tree_cnt; // tree: [0] groups done, [1 + g] CTAs of group g done (zero between calls)
     float2 *group_totals;   // tree: [ceil(P / kTreeGroup)][H] (hi, lo)
+    unsigned int *grid_cnt; // grid: CTA arrivals at the barrier (zero between calls)
+    unsigned int *grid_gen; // grid: barrier generation (advances every call)
     unsigned int *arrivals; // single: CTA arrival counter (zero between calls)
     int block_rows;     // blocked accumulation: rows per FP32 block
     int *status;

@@ -184,7 +184,10 @@ typedef enum {
 typedef struct {
     int single;        /* 0: main + fixed-order reduce pair; 1: single kernel,
                           FP64 atomics; 2: single kernel, fixed-order reduce
-                          by the last-arriving CTAs (deterministic) */
+                          by the last-arriving CTAs (deterministic); 3:
+                          single cooperative kernel, a grid barrier, then a
+                          fixed-order reduce of a column slice by every CTA
+                          (deterministic) */
     int dw_accum;      /* cake_dw_accum */
     int vec_per_thread; /* 16-byte vectors of a row held by each thread */
     int warps_per_row; /* warps that share one row */
@@ -198,11 +201,12 @@ typedef struct {
 
 /*
  * Fill *out with the variant the window table picks for this shape, weight
- * dtype, mode and residual gradient.  force_single (0, 1 or 2 as in
+ * dtype, mode and residual gradient.  force_single (0 to 3 as in
  * cake_variant.single) / force_accum (-1 = let the table decide) override
  * the table, as the tests that sweep every variant do; deterministic = 1
  * refuses force_single = 1 with CAKE_ERR_INVALID; force_single = 2 needs the
- * 8-columns-per-thread layout (H <= 6144), else CAKE_ERR_UNSUPPORTED.
+ * 8-columns-per-thread layout with one row per group (H <= 6144 except
+ * 3080 .. 5120), else CAKE_ERR_UNSUPPORTED.
  */
 cake_status cake_rmsnorm_bwd_select(const cake_shape *shape, cake_dtype w_dtype,
                                     int deterministic, int has_dh, int force_single,
@@ -226,7 +230,7 @@ cake_status cake_rmsnorm_bwd_forced(const cake_shape *shape, const cake_tensor *
  * cake_rmsnorm_bwd_noalloc is the non-deterministic backward (the single
  * kernel, dx identical to cake_rmsnorm_bwd) with its scratch -- the CTA
  * arrival counter and the FP64 column accumulators -- in a library-owned
- * device array of 256 + 8 * CAKE_NOALLOC_MAX_HIDDEN bytes (64.25 KiB), which
+ * device array of 512 + 8 * CAKE_NOALLOC_MAX_HIDDEN bytes (64.5 KiB), which
  * every GPU that loads the library holds until the process exits.  The
  * caller still passes every input and output (same meaning as
  * cake_rmsnorm_bwd).  It allocates nothing and frees nothing.

@@ -73,7 +73,11 @@ def test_select_is_a_valid_launch(cake, H, T):
         assert v["vec_per_thread"] * 32 * v["warps_per_row"] * 8 >= H
         assert v["ctas"] * v["rows_per_cta"] >= T and (v["ctas"] - 1) * v["rows_per_cta"] < T
         assert v["ctas"] <= 152 * 4
-        assert v["single"] == (0 if det else 1)
+        # both modes run the pair (no single-kernel form beats it on GB300)
+        assert v["single"] == 0
+    # the non-deterministic mode still offers every single-kernel form
+    for form in (1, 3):
+        assert cake.cake_rmsnorm_bwd_select((T, 1, H), deterministic=False, force_single=form)["single"] == form
 
 
 def test_row_layout_depends_on_h_alone(cake):

@@ -143,7 +143,7 @@ def test_fwd_empty(cake):
 
 # --------------------------------------------------------------------- bwd
 
-VARIANTS = [(f, acc) for f in (0, 1, 2) for acc in (0, 1, 2, 3)]
+VARIANTS = [(f, acc) for f in (0, 1, 2, 3) for acc in (0, 1, 2, 3)]
 
 
 def oracle_bwd_inputs(x, w, eps, residual=None):
@@ -181,7 +181,7 @@ def check_bwd(cake, x, dy, w, eps, residual=None, dh=None, variants=VARIANTS, dw
     dx_ref_bits = None
     worst = 0.0
     for single, acc in variants:
-        det = single != 1  # the pair and the one-kernel tree are deterministic
+        det = single != 1  # the pair, the tree and the grid form are deterministic
         outs = []
         for rep in range(2):
             try:
@@ -279,14 +279,33 @@ def test_single_kernel_leaves_workspace_clean(cake):
     ws = cake.cake_rmsnorm_bwd_workspace(x, w.dtype, deterministic=False)
     first = None
     for _ in range(5):
-        _, dw = cake.cake_rmsnorm_bwd(dy, x, r, w, deterministic=False, workspace=ws)
+        _, dw = cake.cake_rmsnorm_bwd_forced(dy, x, r, w, deterministic=False, force_single=1, workspace=ws)
         torch.cuda.synchronize()
         if first is None:
             first = dw.clone()
         # FP64 accumulation: repeated calls agree to FP32 rounding of the same sum
         assert torch.allclose(dw, first, rtol=1e-6, atol=1e-6)
-    head = ws[: 256 + 8 * 2048 * 8].cpu()  # arrival counter and the 8 accumulator banks
+    head = ws[: 512 + 8 * 2048 * 8].cpu()  # the counters and the 8 accumulator banks
     assert not head.any()
+
+
+def test_grid_form_barrier_words(cake):
+    # the cooperative form's barrier leaves its counter at zero and advances
+    # its generation once per call; dw is the same bits every call
+    c = cake_inputs.plain_case(900, 1536, seed=12)
+    rin, _ = oracle_bwd_inputs(c["x"], c["w"], c["eps"])
+    x, dy, w, r = c["x"].to(DEV), c["dy"].to(DEV), c["w"].to(DEV), torch.from_numpy(rin).to(DEV)
+    ws = cake.cake_rmsnorm_bwd_workspace(x, w.dtype, deterministic=True)
+    first = None
+    for call in range(3):
+        _, dw = cake.cake_rmsnorm_bwd_forced(dy, x, r, w, deterministic=True, force_single=3, workspace=ws)
+        torch.cuda.synchronize()
+        words = ws[:512].cpu().view(torch.int32)
+        assert int(words[64]) == 0 and int(words[65]) == call + 1
+        if first is None:
+            first = dw.clone()
+        assert torch.equal(dw, first)
+    assert cake.cake_rmsnorm_device_status() == 0
 
 
 @pytest.mark.parametrize("H", [8, 256, 512, 1536, 2048, 4096, 5120, 6144, 8192])

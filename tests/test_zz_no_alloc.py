@@ -4,8 +4,8 @@ Callers that cannot allocate device memory for the library (inside a
 framework that owns every allocation, or on a path that must not call
 cudaMalloc mid-step) use cake_rmsnorm_bwd_noalloc, whose scratch is a device
 array owned by the library.  These checks call it through the C ABI twice in
-a row and compare it with the workspace-taking entry point
-(cake_rmsnorm_bwd, non-deterministic mode, which runs the same kernel):
+a row and compare it with the workspace-taking entry point running the same
+kernel (cake_rmsnorm_bwd_forced, non-deterministic, the single kernel):
 dx within one BF16 step (it is in fact the same bits) and dw within the
 per-element budget the parity tests use.  The file is named to run last, and
 it passes on its own in a fresh process as well as after the other tests.
@@ -49,7 +49,7 @@ def test_noalloc_matches_workspace_entry_point(cake, kind):
     x, dy, w = c["x"], c["dy"], c["w"]
     H = x.shape[-1]
     _, rstd = cake.cake_rmsnorm_fwd(x, w, c["eps"])
-    ref_dx, ref_dw = cake.cake_rmsnorm_bwd(dy, x, rstd, w, deterministic=False)
+    ref_dx, ref_dw = cake.cake_rmsnorm_bwd_forced(dy, x, rstd, w, deterministic=False, force_single=1)
     torch.cuda.synchronize()
     dx = torch.empty(x.shape, dtype=torch.bfloat16, device=DEV)
     dw = torch.empty(H, dtype=torch.float32, device=DEV)
