@@ -140,6 +140,9 @@ WORKLOADS = {
     # T=32768 per-head views, FP32 shared w[256].
     "heads24_t32768_strided": dict(kind="heads", T=32768, heads=24, strided=True, w_dtype=torch.float32),
     "heads4_t32768": dict(kind="heads", T=32768, heads=4, strided=False, w_dtype=torch.float32),
+    # The accuracy sweep's widths at its T = 65536 point (x, dy ~ N(0, 1), BF16 weight), for timing.
+    "h4096_t65536_sweep": dict(kind="plain", T=65536, H=4096, family="gauss", w_dtype=torch.bfloat16, dy_std=1.0),
+    "h5120_t65536_sweep": dict(kind="plain", T=65536, H=5120, family="gauss", w_dtype=torch.bfloat16, dy_std=1.0),
 }
 
 # Accuracy sweep: H x T x weight dtype x input family, 60 seeds per family.
