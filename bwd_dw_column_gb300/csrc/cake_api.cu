@@ -803,7 +803,7 @@ cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, i
         return st;
     const int threads = 32 * (plan.groups * plan.rl.W + 1);
     int n = 0;
-    cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.rpg, plan.single, plan.dwm, threads, plan.smem, &n)
+    cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.rl.W, plan.rpg, plan.single, plan.dwm, threads, plan.smem, &n)
                              : occupancy_fwd(plan.rl.vpt, threads, plan.smem, &n);
     if (e != cudaSuccess)
         return CAKE_ERR_CUDA;

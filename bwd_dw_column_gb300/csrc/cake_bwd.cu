@@ -58,14 +58,14 @@ static cudaError_t status_ptr(int **out)
     return cudaSuccess;
 }
 
-template <int VPT, int DWM, int FORM, int R2, bool KEEP>
+template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1>
 __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const Layout &L = p.L;
     const Smem s = carve_smem(smem_raw, L);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int W = L.warps_per_row;
+    const int W = W1 ? 1 : L.warps_per_row; // W1: rows of one warp, known at compile time
     const int consumer_warps = L.groups * W;
     const Chunk c = cta_chunk(L);
 
@@ -199,7 +199,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                 dot[i] = __fadd_rn(dot2.x, dot2.y);
             }
             float tot[R2];
-            group_sum_n<R2>(dot, tot, s, L, gid, wig, lane, slot++, abort);
+            group_sum_n<R2, W1 ? 1 : 0>(dot, tot, s, L, gid, wig, lane, slot++, abort);
 
 #pragma unroll
             for (int i = 0; i < R2; ++i) {
@@ -483,14 +483,16 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 
 // The row kernels, by row build RB: 0 one row per group; two rows per group
 // (one group and the producer per CTA) keeping x and dy*w in registers for
-// CTAs of up to 17 (1) or 20 (2) warps, or re-reading them for 21 warps (3).
-// The bounds cap the registers a thread may use so that the largest CTA
-// fits: 72 (26 warps), 96 (17 or 20 warps), 80 (21 warps), 128 (13 warps).
+// CTAs of up to 17 (1) or 20 (2) warps, or re-reading them for 21 warps (3);
+// 4 one row per group for rows of one warp (H <= 256), with that width known
+// to the compiler.  The bounds cap the registers a thread may use so that
+// the largest CTA fits: 72 (26 warps), 96 (17 or 20 warps), 80 (21 warps),
+// 128 (13 warps).
 template <int VPT, int DWM, int FORM, int RB>
-__global__ void __launch_bounds__(RB == 0 ? kMaxThreadsFor(VPT) : kRowBuildThreads[RB], 1)
+__global__ void __launch_bounds__(RB == 0 || RB == 4 ? kMaxThreadsFor(VPT) : kRowBuildThreads[RB], 1)
     bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
-    bwd_rows<VPT, DWM, FORM, RB == 0 ? 1 : 2, RB != 3>(p);
+    bwd_rows<VPT, DWM, FORM, RB == 0 || RB == 4 ? 1 : 2, RB != 3, RB == 4>(p);
 }
 
 // Row build of a two-rows-per-group CTA of `threads` threads.
@@ -628,6 +630,8 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
         default: return cudaErrorInvalidValue;
         }
     }
+    if (vpt == 1 && q.L.warps_per_row == 1)
+        return launch_vpt<1, 4>(q, single, dwm, ctas, smem, stream);
     switch (vpt) {
     case 1: return launch_vpt<1, 0>(q, single, dwm, ctas, smem, stream);
     case 2: return launch_vpt<2, 0>(q, single, dwm, ctas, smem, stream);
@@ -686,7 +690,7 @@ static cudaError_t occ_vpt(int single, int dwm, int threads, size_t smem, int *n
     return occ_form<VPT, kFormPair, RB>(dwm, threads, smem, n);
 }
 
-cudaError_t occupancy_bwd(int vpt, int rpg, int single, int dwm, int threads, size_t smem, int *n)
+cudaError_t occupancy_bwd(int vpt, int w, int rpg, int single, int dwm, int threads, size_t smem, int *n)
 {
     if (single == kFormTree)
         return vpt == 1 && rpg == 1 ? occ_form<1, kFormTree, 0>(dwm, threads, smem, n) : cudaErrorInvalidValue;
@@ -700,6 +704,8 @@ cudaError_t occupancy_bwd(int vpt, int rpg, int single, int dwm, int threads, si
         default: return cudaErrorInvalidValue;
         }
     }
+    if (vpt == 1 && w == 1)
+        return occ_vpt<1, 4>(single, dwm, threads, smem, n);
     switch (vpt) {
     case 1: return occ_vpt<1, 0>(single, dwm, threads, smem, n);
     case 2: return occ_vpt<2, 0>(single, dwm, threads, smem, n);

@@ -165,7 +165,7 @@ __device__ __forceinline__ float group_sum(float v, const Smem &s, const Layout 
 
 // group_sum for N rows at once: the N butterflies interleave, and with
 // W > 1 one barrier serves all N rows.  Same order per row as group_sum.
-template <int N>
+template <int N, int WC = 0>
 __device__ __forceinline__ void group_sum_n(const float (&v)[N], float (&out)[N], const Smem &s,
                                             const Layout &L, int gid, int wig, int lane, uint32_t slot,
                                             bool &abort)
@@ -178,7 +178,7 @@ __device__ __forceinline__ void group_sum_n(const float (&v)[N], float (&out)[N]
 #pragma unroll
         for (int n = 0; n < N; ++n)
             out[n] += __shfl_xor_sync(0xffffffffu, out[n], o);
-    const int W = L.warps_per_row;
+    const int W = WC ? WC : L.warps_per_row; // WC: rows of WC warps known at compile time
     if (W == 1) {
         abort = __any_sync(0xffffffffu, abort);
         return;
