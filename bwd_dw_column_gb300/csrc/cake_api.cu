@@ -112,9 +112,10 @@ static RowLayout layout_for(int H, int vpt)
 // reduction order of every per-row sum.  It depends on H (and on whether it
 // is the forward or the backward) alone, so dx, y and rstd are the same bits
 // whatever else the table picks.
-//   backward: 8 columns per thread up to H = 6144 -- the backward keeps
-//     x, dy*w and the dw accumulators of its columns in registers, so few
-//     columns per thread leave room for many resident warps;
+//   backward: 8 columns per thread up to H = 6144 except 24 for 4096 < H
+//     <= 5376 -- the backward keeps x, dy*w and the dw accumulators of its
+//     columns in registers, so few columns per thread leave room for many
+//     resident warps;
 //   forward: 16 columns per thread from H = 512 (fewer, longer rows per
 //     thread amortise the per-row reduction).
 static RowLayout row_layout(int H, Kind kind)
@@ -128,6 +129,12 @@ static RowLayout row_layout(int H, Kind kind)
     const int nvec = H / 8;
     if (nvec <= 32)
         return {1, 1};
+    // backward, 4096 < H <= 5376: 24 columns per thread on 6 or 7 warps,
+    // which leaves room for a second row group or a second CTA per SM
+    // (GB300, T = 65536: H = 4608 det 5 %, H = 4864 3 %, H = 5120 10 % faster
+    // than 8 columns per thread on 18 - 20 warps)
+    if (kind == kBwd && nvec > 32 * 16 && nvec <= 32 * 3 * 7)
+        return layout_for(H, 3);
     if (kind == kBwd && nvec <= 32 * 24)
         return layout_for(H, 1);
     // forward: 16 columns per thread up to H = 4096, then 24 (measured on
@@ -216,9 +223,9 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &gro
 
 // Rows a row group owns per stage: two (interleaved, one barrier for both)
 // where a row is so wide that only one group of its warps fits a CTA (13 to
-// 20 warps: H = 3080 .. 5120), so that two rows are in flight per SM instead
-// of one (GB300, T = 65536: H = 3584 det 16 % faster, H = 4096 19 %, H =
-// 4608 10 %, H = 5120 6 %).  Otherwise one, and more groups per CTA.
+// 16 warps: H = 3080 .. 4096), so that two rows are in flight per SM instead
+// of one (GB300, T = 65536: H = 3584 det 16 %, H = 4096 19 % faster).
+// Otherwise one, and more groups per CTA instead.
 static int rows_per_group(const RowLayout &rl, Kind kind)
 {
     int rpg = 1;

@@ -481,27 +481,17 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     }
 }
 
-// The row kernels, by row build RB: 0 one row per group; two rows per group
-// (one group and the producer per CTA) keeping x and dy*w in registers for
-// CTAs of up to 17 (1) or 20 (2) warps, or re-reading them for 21 warps (3);
-// 4 one row per group for rows of one warp (H <= 256), with that width known
-// to the compiler.  The bounds cap the registers a thread may use so that
-// the largest CTA fits: 72 (26 warps), 96 (17 or 20 warps), 80 (21 warps),
-// 128 (13 warps).
+// The row kernels, by row build RB: 0 one row per group; 1 two rows per
+// group (one group of up to 16 warps and the producer per CTA), keeping x and
+// dy*w of both rows in registers; 4 one row per group for rows of one warp
+// (H <= 256), with that width known to the compiler.  The bounds cap the
+// registers a thread may use so that the largest CTA fits: 72 (26 warps),
+// 96 (17 warps), 128 (13 warps).
 template <int VPT, int DWM, int FORM, int RB>
-__global__ void __launch_bounds__(RB == 0 || RB == 4 ? kMaxThreadsFor(VPT) : kRowBuildThreads[RB], 1)
+__global__ void __launch_bounds__(RB == 1 ? kMaxThreadsR2 : kMaxThreadsFor(VPT), 1)
     bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
-    bwd_rows<VPT, DWM, FORM, RB == 0 || RB == 4 ? 1 : 2, RB != 3, RB == 4>(p);
-}
-
-// Row build of a two-rows-per-group CTA of `threads` threads.
-static int two_row_build(int threads)
-{
-    for (int rb = 1; rb <= 3; ++rb)
-        if (threads <= kRowBuildThreads[rb])
-            return rb;
-    return 0;
+    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4>(p);
 }
 
 // Fixed-order reduction of the pair's CTA partials.  A CTA owns C columns
@@ -623,12 +613,9 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
     if (q.L.rows_per_group == 2) {
         if (vpt != 1)
             return cudaErrorInvalidValue;
-        switch (two_row_build(32 * (q.L.groups * q.L.warps_per_row + 1))) {
-        case 1: return launch_vpt<1, 1>(q, single, dwm, ctas, smem, stream);
-        case 2: return launch_vpt<1, 2>(q, single, dwm, ctas, smem, stream);
-        case 3: return launch_vpt<1, 3>(q, single, dwm, ctas, smem, stream);
-        default: return cudaErrorInvalidValue;
-        }
+        if (32 * (q.L.groups * q.L.warps_per_row + 1) > kMaxThreadsR2)
+            return cudaErrorInvalidValue;
+        return launch_vpt<1, 1>(q, single, dwm, ctas, smem, stream);
     }
     if (vpt == 1 && q.L.warps_per_row == 1)
         return launch_vpt<1, 4>(q, single, dwm, ctas, smem, stream);
@@ -697,12 +684,9 @@ cudaError_t occupancy_bwd(int vpt, int w, int rpg, int single, int dwm, int thre
     if (rpg == 2) {
         if (vpt != 1)
             return cudaErrorInvalidValue;
-        switch (two_row_build(threads)) {
-        case 1: return occ_vpt<1, 1>(single, dwm, threads, smem, n);
-        case 2: return occ_vpt<1, 2>(single, dwm, threads, smem, n);
-        case 3: return occ_vpt<1, 3>(single, dwm, threads, smem, n);
-        default: return cudaErrorInvalidValue;
-        }
+        if (threads > kMaxThreadsR2)
+            return cudaErrorInvalidValue;
+        return occ_vpt<1, 1>(single, dwm, threads, smem, n);
     }
     if (vpt == 1 && w == 1)
         return occ_vpt<1, 4>(single, dwm, threads, smem, n);

@@ -19,14 +19,11 @@ __host__ __device__ constexpr unsigned weight_smem_bytes(int H) { return ((unsig
 // vectors per thread is compiled for; it caps the registers per thread at
 // 65536 / threads.
 __host__ __device__ constexpr int kMaxThreadsFor(int vpt) { return vpt == 1 ? 832 : 416; }
-// Largest CTAs of the backward builds whose groups own two rows per stage
-// (one group and the producer), by row build 1..3 (index 0 unused).  A CTA's
-// warps spread over the SM's four register files of 16384: 17 to 20 warps
-// (5 per file) leave 96 registers a thread, 21 warps (6) only 80 -- too few
-// to keep x and dy*w of two rows in registers, so build 3 re-reads them.  The
-// 17-warp bound schedules better than the 20-warp one (GB300, H = 4096: 6 %).
-constexpr int kRowBuildThreads[4] = {0, 544, 640, 672};
-constexpr int kMaxThreadsR2 = 672;
+// Largest CTA of the backward build whose groups own two rows per stage (one
+// group of up to 16 warps and the producer).  A CTA's warps spread over the
+// SM's four register files of 16384, so its 17 warps (5 per file) leave 96
+// registers a thread.
+constexpr int kMaxThreadsR2 = 544;
 // Named barriers: 1 + g for row group g when a row spans several warps, and
 // the consumer-wide barrier after them (hardware barrier ids are 0..15).  A
 // plan whose rows span several warps has at most kMaxRowGroupBarriers groups.

@@ -206,7 +206,7 @@ typedef struct {
  * the table, as the tests that sweep every variant do; deterministic = 1
  * refuses force_single = 1 with CAKE_ERR_INVALID; force_single = 2 needs the
  * 8-columns-per-thread layout with one row per group (H <= 6144 except
- * 3080 .. 5120), else CAKE_ERR_UNSUPPORTED.
+ * 3080 .. 5376), else CAKE_ERR_UNSUPPORTED.
  */
 cake_status cake_rmsnorm_bwd_select(const cake_shape *shape, cake_dtype w_dtype,
                                     int deterministic, int has_dh, int force_single,

@@ -205,8 +205,8 @@ def test_row_groups_fit_named_barriers(cake):
             if v["warps_per_row"] > 1:
                 assert v["row_groups"] <= 14
             # consumer warps + the producer within the kernel's largest CTA
-            # (832 threads; 672 for two rows per group)
-            assert v["row_groups"] * v["warps_per_row"] + 1 <= (26 if v["rows_per_group"] == 1 else 21)
+            # (832 threads; 544 for two rows per group)
+            assert v["row_groups"] * v["warps_per_row"] + 1 <= (26 if v["rows_per_group"] == 1 else 17)
 
 
 @pytest.mark.parametrize("tune", ["groups=12", "groups=24", "groups=12,cps=1"])
