@@ -299,11 +299,12 @@ static void pick_variant(uint32_t rows, int deterministic, int &single, int &dwm
 }
 
 // Partial ranges per column per warp of the fixed-order reduce: about one
-// CTA per SM or more where H allows, so that each lane sums few partials.
-static int reduce_slices(int H)
+// CTA per SM or more where H allows, and at most 8 partials per lane (one
+// round of loads in flight).
+static int reduce_slices(int H, int P)
 {
     int S = 1;
-    while (S < 8 && (H + 32 / S - 1) / (32 / S) < kSMs)
+    while (S < 8 && ((H + 32 / S - 1) / (32 / S) < kSMs || (P + 16 * S - 1) / (16 * S) > 8))
         S *= 2;
     return S;
 }
@@ -538,7 +539,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     cudaError_t e = launch_bwd_rows(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s);
     if (e != cudaSuccess || plan.single != kFormPair || phase == kMainOnly)
         return cuda_status(e);
-    ReduceParams rp{p.partials, plan.ctas, H, dw, reduce_slices(H)};
+    ReduceParams rp{p.partials, plan.ctas, H, dw, reduce_slices(H, plan.ctas)};
     return cuda_status(launch_dw_reduce(rp, s));
 }
 
@@ -786,7 +787,7 @@ cake_status cake_rmsnorm_bwd_reduce(const cake_shape *shape, int has_dh, float *
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return CAKE_ERR_UNSUPPORTED;
     const float2 *parts = reinterpret_cast<const float2 *>(static_cast<uint8_t *>(workspace) + ws_part_off(H));
-    ReduceParams rp{parts, plan.ctas, H, dw, reduce_slices(H)};
+    ReduceParams rp{parts, plan.ctas, H, dw, reduce_slices(H, plan.ctas)};
     return cuda_status(launch_dw_reduce(rp, s));
 }
 

@@ -39,6 +39,7 @@ from tests import tolerances as tol  # noqa: E402
 FORMS = [  # (name, force_single, force_accum, deterministic)
     ("pair_plain", 0, 0, True), ("pair_blocked", 0, 1, True), ("pair_kahan", 0, 3, True),
     ("pair_twosum", 0, 2, True), ("single_kahan", 1, 3, False), ("single_twosum", 1, 2, False),
+    ("grid_kahan", 3, 3, True),
     ("default_det", None, None, True), ("default_nondet", None, None, False),
 ]
 
