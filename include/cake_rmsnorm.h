@@ -109,9 +109,10 @@ cake_status cake_rmsnorm_fwd(const cake_shape *shape, const cake_tensor *x,
 
 /*
  * Bytes of workspace cake_rmsnorm_bwd needs for this shape and mode
- * (0 only for T = 0).  The workspace holds the CTA partials of the
- * deterministic pair and the FP64 column accumulators and arrival counter of
- * the single kernel, in separate regions.
+ * (0 only for T = 0): enough for every form the call may run.  The workspace
+ * holds, in separate regions, the counters of the one-kernel forms, the FP64
+ * column accumulators of the atomic single kernel, the CTA partials of the
+ * pair and of the grid form, and the tree form's group totals.
  */
 size_t cake_rmsnorm_bwd_workspace_size(const cake_shape *shape, cake_dtype w_dtype,
                                        int deterministic);
@@ -134,9 +135,11 @@ cake_status cake_rmsnorm_bwd_workspace_init(void *workspace, size_t workspace_by
  * dx: output rows (may not alias dy, x or dh).  dw: [H] FP32, overwritten.
  * deterministic != 0: the main + fixed-order reduce pair; dw is bitwise
  * reproducible for equal inputs and shape.  deterministic == 0: the window
- * table may pick the single kernel (FP64 column accumulation in L2 atomics);
- * dw is then not bitwise reproducible.  dx is the same bits in every mode and
- * variant.  T = 0: dw is zero-filled and CAKE_OK returned.
+ * table may pick a single-kernel form where one is faster than the pair, and
+ * dw is then not guaranteed bitwise reproducible; on GB300 none is faster at
+ * any measured shape, so the table runs the pair in both modes
+ * (cake_rmsnorm_bwd_forced selects a single kernel).  dx is the same bits in
+ * every mode and variant.  T = 0: dw is zero-filled and CAKE_OK returned.
  */
 cake_status cake_rmsnorm_bwd(const cake_shape *shape, const cake_tensor *dy,
                              const cake_tensor *x, const float *rstd, const void *w,
