@@ -7,27 +7,32 @@
 //   dx_j = bf16(rstd * (g_j - xhat_j * c) [+ dh_j]),
 // and over rows, the FP32 column sum dw_j = sum_r dy_rj * h_rj * rstd_r.
 //
-// Two backward forms, as the pages describe them:
-//   * the deterministic pair (#8577 commit, intro: "the main kernel +
-//     fixed-order dw reduce"): `bwd_rows_kernel<..., SINGLE=false>` writes one
+// The two backward forms the pages describe, and two more one-kernel forms:
+//   * the deterministic pair (#8577 commit, intro: a main kernel, then a
+//     fixed-order dw reduce): `bwd_rows_kernel<..., FORM=0, ...>` writes one
 //     compensated (hi, lo) dw partial per CTA into the workspace, then
 //     `dw_reduce_kernel` sums the partials of each column in a fixed order
 //     (programmatic dependent launch hides its launch);
 //   * the single kernel (#8208 page, description: FP64 dw column sums, not
-//     bitwise reproducible): `bwd_rows_kernel<..., SINGLE=true>` adds each
-//     CTA's partial into FP64 column accumulators with L2 atomics; the CTA that
-//     arrives last converts them to FP32 dw and zeroes the accumulators and the
-//     arrival counter for the next call.  Nobody waits for anybody.
+//     bitwise reproducible): FORM=1 adds each CTA's partial into FP64 column
+//     accumulators with L2 atomics; the CTA that arrives last converts them to
+//     FP32 dw and zeroes the accumulators and the arrival counter for the next
+//     call.  Nobody waits for anybody;
+//   * the tree form (FORM=2): the last CTA of each group of CTAs sums its
+//     group's partials, and the last group the group totals, in fixed order;
+//   * the grid form (FORM=3): a cooperative launch whose CTAs meet at one
+//     bounded grid barrier, then each reduces a slice of the columns in fixed
+//     order.
 // dx is computed by the same code in every form, with a reduction order fixed
 // by the row layout (VPT, W) alone, so it is bitwise identical across modes,
-// variants and calls (#8208 page, description; #8253 commit: "dx is bitwise
-// identical across every one" of the window edges).
+// variants and calls (#8208 page, description; the #8253 commit states that
+// dx does not change across the window edges).
 //
 // Per-thread dw accumulation over the CTA's rows (DWM), the pages' kernel
 // kinds restated: plain FP32 sums; blocked FP32 sums folded into a
 // compensated pair ("kb", PR #8899 page, window list); TwoSum per-thread sums
 // with the product's rounding error kept (#8208 page, description; #8253
-// commit: "the twosum forms").
+// commit, which names the TwoSum forms).
 #include <mutex>
 
 #include "cake_launch.h"

@@ -10,7 +10,8 @@
 // One program serves both backward modes (#8253 commit: the forward is the
 // same in both, so y, rstd and h_new are bitwise equal across modes); the
 // sum of squares has a reduction order fixed by the row layout, so a
-// recomputed forward (the checkpointed "2xfwd+bwd" step) is bitwise equal.
+// recomputed forward (a checkpointed step runs the forward again before the
+// backward) is bitwise equal.
 #include <mutex>
 
 #include "cake_launch.h"

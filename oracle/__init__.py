@@ -13,7 +13,8 @@ passage it follows in the C source's header:
   GB300 windows" commit (#8577) quoted on the PR #8208 page, intro;
 * residual route returns h_new and normalises it: same commit, "Key";
 * per-head views with one shared w[256]: PR #8208 page, description;
-* dw "against FP64 at the kernel's FP32 rstd": PR #8208 page, description.
+* dw is checked against FP64 computed at the kernel's FP32 rstd: PR #8208
+  page, description.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (finite differences, closed forms, exact sums, invariants, reductions to

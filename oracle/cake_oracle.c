@@ -18,8 +18,8 @@
  *     and normalises it -- #8577 commit, "Key" (`res`).
  *   - per-head views [T,24,256] with strides (12288,512,1) and [T,4,256] with
  *     one shared w[256]: PR #8208 page, description.
- *   - dw is checked "against FP64 at the kernel's FP32 rstd": PR #8208 page,
- *     description.  So every function here that produces y, dx or dw takes the
+ *   - dw is checked against an FP64 result computed at the kernel's FP32
+ *     rstd: PR #8208 page, description.  So every function here that produces y, dx or dw takes the
  *     rstd to use as an input (the kernel's FP32 value, widened to double).
  *
  * Row r of a [T, nh, H] view is (t, k) = (r / nh, r % nh); element j of that
