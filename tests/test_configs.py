@@ -9,6 +9,8 @@ benchmark times (the default window table, both backward modes).
   computes them one row at a time).
 * Per-head views at T=32768 ([T,24,256] strided slice of [T,24,512], and
   contiguous [T,4,256]): every row and column.
+* The accuracy sweep's widths H=4096 and H=5120 at T=65536: rstd of every
+  row, dw of every column, y and dx of sampled rows.
 
 Inputs are drawn on the device from seeded generators and copied to the host
 for the oracle.  The backward's rstd (and on the residual route its h_new)
@@ -154,3 +156,11 @@ def test_h6144_t131072_residual(cake):
 def test_per_head(cake, name):
     c = cake_inputs.make(name, seed=0, device=DEV)
     run_workload(cake, c["x"], c["dy"], c["w"], c["eps"])
+
+
+@pytest.mark.parametrize("name", ["h4096_t65536_sweep", "h5120_t65536_sweep"])
+def test_sweep_widths(cake, name):
+    # the accuracy sweep's widths at T = 65536: two rows per group (H = 4096)
+    # and 24 columns per thread (H = 5120); dx of sampled rows, dw of every column
+    c = cake_inputs.make(name, seed=0, device=DEV)
+    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], full_dx=False)
