@@ -190,12 +190,15 @@ static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int warps_per_ct
 // 7 % faster as 3 groups, and the fewer CTA partials shorten the dw
 // reduction).  Otherwise about 8 consumer warps per CTA, then as many CTAs
 // per SM as the register file holds (at most 3).
-static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &groups, int &ctas_per_sm)
+static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int ntens, int &groups,
+                      int &ctas_per_sm)
 {
     const int W = rl.W;
     const int max_warps = (rpg == 2 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
     if (kind == kBwd && W > 1)
         groups = max_warps / W > 1 ? max_warps / W : 1;
+    else if (kind == kFwd && ntens == 1 && rl.vpt == 2 && W > 1)
+        groups = max_warps / W > 1 ? max_warps / W : 1; // plain forward: see the cap below
     else
         groups = W >= 8 ? 1 : 8 / W;
     const Tune &t = tune();
@@ -213,6 +216,15 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int &gro
         cap = 4;
     else if (kind == kFwd && W > 1 && W <= 4)
         cap = 2;
+    // plain forward at 16 columns per thread (H = 1024 .. 4096): two CTAs of
+    // about 12 consumer warps (GB300, T = 65536: H = 1024 15 %, H = 1536 22 %,
+    // H = 2048 2 %, H = 4096 4 % faster than the earlier 8-warp CTAs);
+    // residual forward at 24 columns on 8 warps (H = 6144): one CTA per SM
+    // (5 % faster)
+    if (kind == kFwd && ntens == 1 && rl.vpt == 2 && W > 1)
+        cap = 2;
+    if (kind == kFwd && ntens == 2 && rl.vpt == 3 && W == 8)
+        cap = 1;
     if (ctas_per_sm > cap)
         ctas_per_sm = cap;
     if (ctas_per_sm < 1)
@@ -245,7 +257,7 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     Plan p;
     p.rl = row_layout(H, kind);
     p.rpg = rows_per_group(p.rl, kind);
-    cta_shape(p.rl, kind, p.rpg, dwm, p.groups, p.ctas_per_sm);
+    cta_shape(p.rl, kind, p.rpg, dwm, ntens, p.groups, p.ctas_per_sm);
     const size_t per_cta = kSmemPerSM / p.ctas_per_sm;
     const size_t stage = (size_t)ntens * p.groups * p.rpg * H * 2;
     const size_t fixed = (size_t)kMiscBytes + weight_smem_bytes(H);
