@@ -104,6 +104,25 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             lo[k][q] = make_float2(0.f, 0.f);
             blk[k][q] = make_float2(0.f, 0.f);
         }
+    // Blocked sums keep their compensation terms in shared memory (this
+    // thread's own slots), so the row loop holds only hi and the block sum.
+    const int nct = consumer_warps * 32;
+    auto lo_add = [&](const float2 (&err)[VPT][4]) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            float4 a = s.lo[(2 * k) * nct + threadIdx.x], b = s.lo[(2 * k + 1) * nct + threadIdx.x];
+            a = make_float4(__fadd_rn(a.x, err[k][0].x), __fadd_rn(a.y, err[k][0].y), __fadd_rn(a.z, err[k][1].x),
+                            __fadd_rn(a.w, err[k][1].y));
+            b = make_float4(__fadd_rn(b.x, err[k][2].x), __fadd_rn(b.y, err[k][2].y), __fadd_rn(b.z, err[k][3].x),
+                            __fadd_rn(b.w, err[k][3].y));
+            s.lo[(2 * k) * nct + threadIdx.x] = a;
+            s.lo[(2 * k + 1) * nct + threadIdx.x] = b;
+        }
+    };
+    if (DWM == CAKE_DWM_BLOCKED)
+#pragma unroll
+        for (int k = 0; k < 2 * VPT; ++k)
+            s.lo[k * nct + threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
     int blk_rows = 0;
 
     // A group owns R2 consecutive rows of every tile: gid*R2 + i.
@@ -251,16 +270,17 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             }
             if (DWM == CAKE_DWM_BLOCKED && (blk_rows += nrow) >= p.block_rows) {
                 blk_rows = 0;
+                float2 err[VPT][4];
 #pragma unroll
                 for (int k = 0; k < VPT; ++k)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        float2 sum, err;
-                        two_sum2(hi[k][q], blk[k][q], sum, err);
+                        float2 sum;
+                        two_sum2(hi[k][q], blk[k][q], sum, err[k][q]);
                         hi[k][q] = sum;
-                        lo[k][q] = add2(lo[k][q], err);
                         blk[k][q] = make_float2(0.f, 0.f);
                     }
+                lo_add(err);
             }
         }
         __syncwarp();
@@ -282,15 +302,24 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     if (abort && lane == 0)
         set_status(p.status, kStatusTimeout);
     if (DWM == CAKE_DWM_BLOCKED) {
+        float2 err[VPT][4];
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                float2 sum, err;
-                two_sum2(hi[k][q], blk[k][q], sum, err);
+                float2 sum;
+                two_sum2(hi[k][q], blk[k][q], sum, err[k][q]);
                 hi[k][q] = sum;
-                lo[k][q] = add2(lo[k][q], err);
             }
+        lo_add(err);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const float4 a = s.lo[(2 * k) * nct + threadIdx.x], b = s.lo[(2 * k + 1) * nct + threadIdx.x];
+            lo[k][0] = make_float2(a.x, a.y);
+            lo[k][1] = make_float2(a.z, a.w);
+            lo[k][2] = make_float2(b.x, b.y);
+            lo[k][3] = make_float2(b.z, b.w);
+        }
     }
     if (FORM == kFormPair)
         pdl_launch_dependents();

@@ -29,6 +29,7 @@ struct Smem {
     float *red;       // [groups][2][R2][W] (groups * W * R2 <= 50: 400 bytes)
     int *flag;        // [4]
     float *wsm;       // [H] the weight as FP32, staged once per CTA
+    float4 *lo;       // blocked dw sums: [2 * VPT][consumer threads] compensation terms
     uint8_t *ring;    // stages * stage_bytes
     uint32_t stage_bytes;
     uint32_t tens_bytes; // bytes of one tensor in one stage
@@ -42,7 +43,8 @@ __device__ __forceinline__ Smem carve_smem(uint8_t *base, const Layout &L)
     s.red = reinterpret_cast<float *>(base + 16 * 2 * 8); // 256 B of barriers first
     s.flag = reinterpret_cast<int *>(base + kMiscBytes - 16);
     s.wsm = reinterpret_cast<float *>(base + kMiscBytes);
-    s.ring = base + kMiscBytes + weight_smem_bytes(L.H);
+    s.lo = reinterpret_cast<float4 *>(base + kMiscBytes + weight_smem_bytes(L.H));
+    s.ring = base + kMiscBytes + weight_smem_bytes(L.H) + L.lo_bytes;
     s.tens_bytes = (uint32_t)L.groups * L.rows_per_group * L.H * 2;
     s.stage_bytes = s.tens_bytes * L.ntens;
     return s;
