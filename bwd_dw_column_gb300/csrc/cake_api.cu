@@ -161,13 +161,14 @@ static size_t ring_smem(int ntens, int rows_per_stage, int H, int stages, size_t
     return (size_t)kMiscBytes + weight_smem_bytes(H) + lo_bytes + (size_t)stages * ntens * rows_per_stage * H * 2;
 }
 
-// Shared memory the blocked dw form keeps its per-thread compensation terms
-// in: 8 floats per vector per consumer thread.
+// Shared memory the blocked dw form keeps its per-thread compensated pair
+// in: the low parts, 8 floats per vector per consumer thread, and with 8
+// columns per thread the high parts as well.
 static size_t lo_smem(Kind kind, int dwm, const RowLayout &rl, int groups)
 {
     if (kind != kBwd || dwm != CAKE_DW_BLOCKED)
         return 0;
-    const size_t n = (size_t)groups * rl.W * 32 * rl.vpt * 32;
+    const size_t n = (size_t)groups * rl.W * 32 * rl.vpt * 32 * (rl.vpt == 1 ? 2 : 1);
     return (n + 1023) & ~size_t(1023);
 }
 

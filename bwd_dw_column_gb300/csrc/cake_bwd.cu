@@ -104,25 +104,61 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             lo[k][q] = make_float2(0.f, 0.f);
             blk[k][q] = make_float2(0.f, 0.f);
         }
-    // Blocked sums keep their compensation terms in shared memory (this
-    // thread's own slots), so the row loop holds only hi and the block sum.
+    // Blocked sums keep the compensated pair in shared memory (this thread's
+    // own slots: planes [0, 2 VPT) the low parts, [2 VPT, 4 VPT) the high
+    // parts with 8 columns per thread), so the row loop holds only the block
+    // sums -- the registers of the plain sum.  Wider layouts keep the high
+    // parts in registers.
+    constexpr bool kHiSmem = DWM == CAKE_DWM_BLOCKED && VPT == 1;
     const int nct = consumer_warps * 32;
-    auto lo_add = [&](const float2 (&err)[VPT][4]) {
+    auto plane = [&](int i) -> float4 & { return s.lo[i * nct + threadIdx.x]; };
+    auto get4 = [&](int i, float2 &a, float2 &b) {
+        const float4 v = plane(i);
+        a = make_float2(v.x, v.y);
+        b = make_float2(v.z, v.w);
+    };
+    auto put4 = [&](int i, float2 a, float2 b) { plane(i) = make_float4(a.x, a.y, b.x, b.y); };
+    // fold the block sums into the pair: (hi, lo) += blk, blk = 0
+    auto fold = [&]() {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            float4 a = s.lo[(2 * k) * nct + threadIdx.x], b = s.lo[(2 * k + 1) * nct + threadIdx.x];
-            a = make_float4(__fadd_rn(a.x, err[k][0].x), __fadd_rn(a.y, err[k][0].y), __fadd_rn(a.z, err[k][1].x),
-                            __fadd_rn(a.w, err[k][1].y));
-            b = make_float4(__fadd_rn(b.x, err[k][2].x), __fadd_rn(b.y, err[k][2].y), __fadd_rn(b.z, err[k][3].x),
-                            __fadd_rn(b.w, err[k][3].y));
-            s.lo[(2 * k) * nct + threadIdx.x] = a;
-            s.lo[(2 * k + 1) * nct + threadIdx.x] = b;
+            float2 h[4], l[4], e[4];
+            if constexpr (kHiSmem) {
+                get4(2 * VPT + 2 * k, h[0], h[1]);
+                get4(2 * VPT + 2 * k + 1, h[2], h[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    h[q] = hi[k][q];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float2 sum;
+                two_sum2(h[q], blk[k][q], sum, e[q]);
+                h[q] = sum;
+                blk[k][q] = make_float2(0.f, 0.f);
+            }
+            get4(2 * k, l[0], l[1]);
+            get4(2 * k + 1, l[2], l[3]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                l[q] = add2(l[q], e[q]);
+            put4(2 * k, l[0], l[1]);
+            put4(2 * k + 1, l[2], l[3]);
+            if constexpr (kHiSmem) {
+                put4(2 * VPT + 2 * k, h[0], h[1]);
+                put4(2 * VPT + 2 * k + 1, h[2], h[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    hi[k][q] = h[q];
+            }
         }
     };
     if (DWM == CAKE_DWM_BLOCKED)
 #pragma unroll
-        for (int k = 0; k < 2 * VPT; ++k)
-            s.lo[k * nct + threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < (kHiSmem ? 4 : 2) * VPT; ++k)
+            plane(k) = make_float4(0.f, 0.f, 0.f, 0.f);
     int blk_rows = 0;
 
     // A group owns R2 consecutive rows of every tile: gid*R2 + i.
@@ -270,17 +306,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             }
             if (DWM == CAKE_DWM_BLOCKED && (blk_rows += nrow) >= p.block_rows) {
                 blk_rows = 0;
-                float2 err[VPT][4];
-#pragma unroll
-                for (int k = 0; k < VPT; ++k)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float2 sum;
-                        two_sum2(hi[k][q], blk[k][q], sum, err[k][q]);
-                        hi[k][q] = sum;
-                        blk[k][q] = make_float2(0.f, 0.f);
-                    }
-                lo_add(err);
+                fold();
             }
         }
         __syncwarp();
@@ -302,23 +328,15 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     if (abort && lane == 0)
         set_status(p.status, kStatusTimeout);
     if (DWM == CAKE_DWM_BLOCKED) {
-        float2 err[VPT][4];
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float2 sum;
-                two_sum2(hi[k][q], blk[k][q], sum, err[k][q]);
-                hi[k][q] = sum;
-            }
-        lo_add(err);
+        fold();
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const float4 a = s.lo[(2 * k) * nct + threadIdx.x], b = s.lo[(2 * k + 1) * nct + threadIdx.x];
-            lo[k][0] = make_float2(a.x, a.y);
-            lo[k][1] = make_float2(a.z, a.w);
-            lo[k][2] = make_float2(b.x, b.y);
-            lo[k][3] = make_float2(b.z, b.w);
+            get4(2 * k, lo[k][0], lo[k][1]);
+            get4(2 * k + 1, lo[k][2], lo[k][3]);
+            if constexpr (kHiSmem) {
+                get4(2 * VPT + 2 * k, hi[k][0], hi[k][1]);
+                get4(2 * VPT + 2 * k + 1, hi[k][2], hi[k][3]);
+            }
         }
     }
     if (FORM == kFormPair)

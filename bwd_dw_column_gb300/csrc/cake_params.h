@@ -70,8 +70,8 @@ struct Layout {
     int groups;         // NG
     int rows_per_group; // rows a group owns per stage (1, or 2 for the backward)
     int stages;         // ring depth
-    int lo_bytes;       // backward, blocked dw sums: the per-thread compensation terms kept in
-                        // shared memory ([2 * VPT float4][consumer threads]); 0 otherwise
+    int lo_bytes;       // backward, blocked dw sums: the per-thread compensated pairs kept in
+                        // shared memory ([2 or 4 * VPT float4][consumer threads]); 0 otherwise
     int ntens;          // tensors staged per row (x[, residual] / x, dy[, dh])
     uint32_t rows;      // total rows R = T * nh
     uint32_t nh;

@@ -29,7 +29,7 @@ struct Smem {
     float *red;       // [groups][2][R2][W] (groups * W * R2 <= 50: 400 bytes)
     int *flag;        // [4]
     float *wsm;       // [H] the weight as FP32, staged once per CTA
-    float4 *lo;       // blocked dw sums: [2 * VPT][consumer threads] compensation terms
+    float4 *lo;       // blocked dw sums: [2 or 4 * VPT][consumer threads] compensated pairs
     uint8_t *ring;    // stages * stage_bytes
     uint32_t stage_bytes;
     uint32_t tens_bytes; // bytes of one tensor in one stage
