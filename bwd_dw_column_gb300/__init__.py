@@ -374,3 +374,12 @@ def cake_rmsnorm_device_status(clear: bool = True) -> int:
     code = ctypes.c_int(0)
     _check(lib.cake_rmsnorm_device_status(ctypes.byref(code), int(bool(clear))), "cake_rmsnorm_device_status")
     return code.value
+
+
+# the training facade (autograd function and the pages' Python names)
+from .train import (CakeRMSNormFunction, cake_rmsnorm, cake_rmsnorm_train_backward,  # noqa: E402
+                    cake_rmsnorm_train_backward_workspace, cake_rmsnorm_train_backward_workspace_bytes,
+                    cake_rmsnorm_train_forward)
+
+__all__ += ["CakeRMSNormFunction", "cake_rmsnorm", "cake_rmsnorm_train_forward", "cake_rmsnorm_train_backward",
+            "cake_rmsnorm_train_backward_workspace_bytes", "cake_rmsnorm_train_backward_workspace"]
