@@ -211,15 +211,52 @@ __device__ __forceinline__ void consumer_sync(const Layout &L)
 // plane 0 holds columns 0-3 of every 8-column vector, plane 1 columns 4-7, so
 // that a warp reading its vectors' weights with 16-byte loads touches
 // consecutive addresses (no bank conflicts).
+template <bool VEC = true>
 __device__ __forceinline__ void stage_weight(const Smem &s, const Layout &L, const void *w, int w_f32)
 {
     const int nthr = 32 * L.groups * L.warps_per_row;
-    const int half = L.nvec * 4;
-    for (int j = threadIdx.x; j < L.H; j += nthr) {
-        const float v = w_f32 ? static_cast<const float *>(w)[j]
-                              : __uint_as_float((uint32_t)static_cast<const uint16_t *>(w)[j] << 16);
-        const int vec = j >> 3, e = j & 7;
-        s.wsm[(e >> 2) * half + vec * 4 + (e & 3)] = v;
+    if (!VEC) { // one element per thread and round
+        const int half = L.nvec * 4;
+        for (int j = threadIdx.x; j < L.H; j += nthr) {
+            const float v = w_f32 ? static_cast<const float *>(w)[j]
+                                  : __uint_as_float((uint32_t)static_cast<const uint16_t *>(w)[j] << 16);
+            const int vec = j >> 3, e = j & 7;
+            s.wsm[(e >> 2) * half + vec * 4 + (e & 3)] = v;
+        }
+        consumer_sync(L);
+        return;
+    }
+    // One 16-byte vector of w (8 BF16) or two (8 FP32) per consumer thread
+    // and round, all loads of a round issued before its stores (w is 16-byte
+    // aligned: the host checks it).
+    constexpr int U = 2;
+    float4 *wsm = reinterpret_cast<float4 *>(s.wsm);
+    for (int v0 = threadIdx.x; v0 < L.nvec; v0 += U * nthr) {
+        float4 a[U], b[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * nthr;
+            if (v < L.nvec) {
+                if (w_f32) {
+                    a[u] = __ldg(static_cast<const float4 *>(w) + 2 * v);
+                    b[u] = __ldg(static_cast<const float4 *>(w) + 2 * v + 1);
+                } else {
+                    const uint4 r = __ldg(static_cast<const uint4 *>(w) + v);
+                    a[u] = make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
+                                       __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+                    b[u] = make_float4(__uint_as_float(r.z << 16), __uint_as_float(r.z & 0xffff0000u),
+                                       __uint_as_float(r.w << 16), __uint_as_float(r.w & 0xffff0000u));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * nthr;
+            if (v < L.nvec) {
+                wsm[v] = a[u];
+                wsm[L.nvec + v] = b[u];
+            }
+        }
     }
     consumer_sync(L);
 }
