@@ -64,11 +64,23 @@ def weight(H: int, gen: torch.Generator, dtype: torch.dtype, device="cpu") -> to
 
 
 def rows_input(T: int, H: int, family: str, gen: torch.Generator, device="cpu") -> torch.Tensor:
-    """x [T, H] BF16 for one input family: 'gauss', 'outlier' or 'offset'."""
+    """x [T, H] BF16 for one input family: 'gauss', 'outlier', 'offset' or
+    'rowmean' (each row r drawn around its own mean m_r = 3 + N(0, 1):
+    x_rj = m_r + N(0, 1), the per-row random-mean reading of the mean-offset
+    family)."""
     if family == "gauss":
         return normal_bf16((T, H), gen, device=device)
     if family == "offset":
         return normal_bf16((T, H), gen, mean=3.0, device=device)
+    if family == "rowmean":
+        means = 3.0 + torch.randn(T, generator=gen, dtype=torch.float32, device=device)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        for a in range(0, T, 8192):
+            b = min(T, a + 8192)
+            t = torch.randn((b - a, H), generator=gen, dtype=torch.float32, device=device)
+            t.add_(means[a:b, None])
+            out[a:b] = t.to(torch.bfloat16)
+        return out
     if family == "outlier":
         n_out = math.ceil(0.01 * T) if T > 0 else 0
         picks = torch.randperm(T, generator=gen, device=device)[:n_out] if T > 0 else None

@@ -377,3 +377,4 @@ def test_bf16_round_ties_and_double_rounding():
     # overflow past the largest finite BF16 plus half an ulp -> inf
     assert oracle.bf16_round(np.array([2.0 ** 128]))[0] == 0x7F80
     assert oracle.bf16_round(np.array([-1e300]))[0] == 0xFF80
+

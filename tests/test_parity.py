@@ -122,7 +122,7 @@ def test_fwd_residual(cake, T, H):
 
 
 def test_fwd_outlier_and_offset_families(cake):
-    for fam in ("outlier", "offset"):
+    for fam in ("outlier", "offset", "rowmean"):
         c = cake_inputs.plain_case(500, 2048, family=fam, w_dtype=torch.float32, seed=3)
         check_fwd(cake, c["x"], c["w"], c["eps"])
 
@@ -228,6 +228,15 @@ BWD_SHAPES = [(1, 8), (2, 16), (3, 24), (37, 256), (5, 520), (300, 1536), (129, 
 def test_bwd_plain(cake, T, H, w_dtype):
     c = cake_inputs.plain_case(T, H, w_dtype=w_dtype, seed=7 * T + H)
     check_bwd(cake, c["x"], c["dy"], c["w"], c["eps"])
+
+
+@pytest.mark.parametrize("family", ["outlier", "offset", "rowmean"])
+@pytest.mark.parametrize("T,H", [(700, 2048), (2500, 1536)])
+def test_bwd_families(cake, family, T, H):
+    # the input families of the accuracy sweep, through every form; 2500 rows
+    # take the blocked dw sums
+    c = cake_inputs.plain_case(T, H, family=family, w_dtype=torch.float32, seed=T + len(family))
+    check_bwd(cake, c["x"], c["dy"], c["w"], c["eps"], variants=[(0, 0), (0, 1), (1, 1), (3, 3)])
 
 
 @pytest.mark.parametrize("T,H", [(3, 256), (300, 1536), (77, 6144)])
