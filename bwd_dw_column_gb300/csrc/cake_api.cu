@@ -344,7 +344,7 @@ static int reduce_slices(int H, int P)
 constexpr size_t kWsHeader = 512;
 constexpr int kTreeMaxGroups = 62;
 constexpr int kGridWords = 64;
-constexpr int kAccBanks = 8;      // copies of the single kernel's FP64 accumulators
+constexpr int kAccBanks = kMaxAccBanks; // copies of the single kernel's FP64 accumulators
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -561,6 +561,10 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     {
         const size_t room = workspace_bytes > kWsHeader ? (workspace_bytes - kWsHeader) / ((size_t)H * 8) : 0;
         p.banks = room >= (size_t)kAccBanks ? kAccBanks : (int)(room > 0 ? room : 1);
+        // CTA b adds into bank b % banks: more banks than CTAs would only
+        // lengthen the last CTA's finalise
+        if (plan.ctas > 0 && p.banks > plan.ctas)
+            p.banks = plan.ctas;
     }
     p.block_rows = 16;
     p.status = nullptr;

@@ -524,11 +524,18 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         __threadfence();
         const int nthr = consumer_warps * 32;
         for (int j = threadIdx.x; j < ncol; j += nthr) {
+            // every bank's load issued before the sum (banks in ascending order)
+            double v[kMaxAccBanks];
+#pragma unroll
+            for (int b = 0; b < kMaxAccBanks; ++b)
+                v[b] = b < p.banks ? __ldcg(p.acc + (size_t)b * ncol + j) : 0.0;
             double sum = 0.0;
-            for (int b = 0; b < p.banks; ++b) {
-                sum += __ldcg(p.acc + (size_t)b * ncol + j);
-                p.acc[(size_t)b * ncol + j] = 0.0;
-            }
+#pragma unroll
+            for (int b = 0; b < kMaxAccBanks; ++b)
+                if (b < p.banks) {
+                    sum += v[b];
+                    p.acc[(size_t)b * ncol + j] = 0.0;
+                }
             p.dw[j] = (float)sum;
         }
         if (threadIdx.x == 0)

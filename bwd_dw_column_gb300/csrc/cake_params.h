@@ -41,6 +41,8 @@ constexpr int kFormAtomic = 1;
 constexpr int kFormTree = 2;
 constexpr int kFormGrid = 3;
 constexpr int kTreeGroup = 16;
+// Copies (banks) of the single kernel's FP64 column accumulators, at most.
+constexpr int kMaxAccBanks = 8;
 
 // Per-thread dw accumulation forms (same values as cake_dw_accum).
 #define CAKE_DWM_PLAIN 0
@@ -107,7 +109,7 @@ struct BwdParams {
     float *dw;          // [H]
     float2 *partials;   // pair: [ctas][H] (hi, lo)
     double *acc;        // single: [banks][H] FP64 column accumulators (zero between calls)
-    int banks;          // single: copies of the accumulators (1..16)
+    int banks;          // single: copies of the accumulators (1..kMaxAccBanks, at most the CTA count)
     unsigned int *tree_cnt; // tree: [0] groups done, [1 + g] CTAs of group g done (zero between calls)
     float2 *group_totals;   // tree: [ceil(P / kTreeGroup)][H] (hi, lo)
     unsigned int *grid_cnt; // grid: CTA arrivals at the barrier (zero between calls)
