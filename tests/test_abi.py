@@ -80,6 +80,23 @@ def test_select_is_a_valid_launch(cake, H, T):
         assert cake.cake_rmsnorm_bwd_select((T, 1, H), deterministic=False, force_single=form)["single"] == form
 
 
+def test_every_width_plans_a_valid_launch(cake):
+    # every supported H (multiples of 8 up to 8192), with and without dh and
+    # for every dw accumulation form: the plan fits the kernel it launches
+    for H in range(8, 8193, 8):
+        for T, dh, acc in ((65536, False, None), (7, True, None), (3000, False, 2), (3000, True, 3)):
+            v = cake.cake_rmsnorm_bwd_select((T, 1, H), deterministic=True, has_dh=dh, force_accum=acc)
+            warps = v["row_groups"] * v["warps_per_row"] + 1
+            bound = 544 if v["rows_per_group"] == 2 else (832 if v["vec_per_thread"] == 1 else 416)
+            assert 32 * warps <= bound, (H, T, v)
+            assert v["smem_bytes"] <= 227 * 1024, (H, T, v)
+            assert 2 <= v["stages"] <= 16, (H, T, v)
+            assert v["vec_per_thread"] * 32 * v["warps_per_row"] * 8 >= H, (H, v)
+            assert v["ctas"] * v["rows_per_cta"] >= T > (v["ctas"] - 1) * v["rows_per_cta"], (H, T, v)
+            if v["warps_per_row"] > 1:
+                assert v["row_groups"] <= 14, (H, v)
+
+
 def test_row_layout_depends_on_h_alone(cake):
     for H in (256, 1536, 2048, 6144):
         layouts = set()
