@@ -105,9 +105,9 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary when it was taken
-    on the current kernel sources; else None."""
+def traffic_record(kernel: str, workload: str):
+    """The committed ncu record (DRAM bytes per launch, the summary file) when
+    it holds for the current kernel sources; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
@@ -116,7 +116,14 @@ def recorded_traffic(kernel: str, workload: str):
     ent = rec.get(f"{kernel}:{workload}")
     if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary when it was taken
+    on the current kernel sources; else None."""
+    ent = traffic_record(kernel, workload)
+    return ent.get("dram_bytes_per_launch") if ent else None
 
 
 class ClockSampler:
@@ -457,6 +464,7 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": round(achieved_main / peak, 4),
             "traffic": recorded_traffic("bwd_rows_kernel", args.workload),
+            "traffic_summary": (traffic_record("bwd_rows_kernel", args.workload) or {}).get("summary"),
             "algorithmic_bytes": nbytes["main"],
         },
         "e2e": {

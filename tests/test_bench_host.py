@@ -76,3 +76,20 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+
+def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
+    import bench
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "s.md").write_text("summary")
+    rec = {"bwd_rows_kernel:w": {"source_hash": h, "dram_bytes_per_launch": 123, "summary": "profiles/s.md"},
+           "bwd_rows_kernel:stale": {"source_hash": "0" * 16, "dram_bytes_per_launch": 456, "summary": "profiles/s.md"}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    assert bench.recorded_traffic("bwd_rows_kernel", "w") == 123
+    assert bench.traffic_record("bwd_rows_kernel", "w")["summary"] == "profiles/s.md"
+    assert bench.recorded_traffic("bwd_rows_kernel", "stale") is None  # counters from other sources
+    assert bench.traffic_record("bwd_rows_kernel", "missing") is None
