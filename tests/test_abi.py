@@ -252,3 +252,34 @@ def test_tree_form_selection(cake):
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), force_single=2)
     groups = (v["ctas"] + 15) // 16
     assert n >= 256 + 8 * 8 * 256 + v["ctas"] * 256 * 8 + groups * 256 * 8
+
+
+C_CLIENT = r"""
+#include "cake_rmsnorm.h"
+#include <stdio.h>
+int main(void) {
+    cake_shape s = {65536, 1, 2048};
+    cake_variant v;
+    cake_status st = cake_rmsnorm_bwd_select(&s, CAKE_FP32, 1, 0, -1, -1, &v);
+    size_t ws = cake_rmsnorm_bwd_workspace_size(&s, CAKE_FP32, 1);
+    cake_shape bad = {4, 1, 12};  /* H not a multiple of 8 */
+    cake_status st_bad = cake_rmsnorm_bwd_select(&bad, CAKE_FP32, 1, 0, -1, -1, &v);
+    printf("%d %zu %d %d %s\n", (int)st, ws, (int)st_bad, cake_rmsnorm_abi_version(), cake_status_str(st_bad));
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(cake, tmp_path):
+    # the boundary needs no C++ and no torch: a C99 client compiles against
+    # the header, links the library and calls its host-only entry points
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                           "-x", "c", HEADER])
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(cake.LIB_PATH)
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                           "-L", libdir, "-lcake_rmsnorm", "-Wl,-rpath," + libdir, "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert out[0] == "0" and int(out[1]) > 0 and out[2] == "2" and out[3] == "1"
