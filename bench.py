@@ -1,10 +1,16 @@
 #!/usr/bin/env python
-"""Benchmark of the training RMSNorm backward on one GB300 (per rank).
+"""Benchmark of the training RMSNorm on one GB300 (per rank).
 
-Default workload: T = 65536 tokens, H = 2048, x BF16 ~ N(0, 1) with 1 % of the
-rows scaled by 30 (outlier family), dy BF16 ~ N(0, 1e-2), w FP32; one step is
-one deterministic backward (main kernel + fixed-order dw reduce) through the
-C ABI.  Printed as one JSON line on rank 0.
+Headline workload (the largest configuration that fits one GPU): T = 131072
+tokens, H = 6144, fused residual add -- x BF16 ~ N(0, 1), residual BF16 ~
+N(0, std 0.5), dy (and dh, the gradient reaching h_new) BF16 ~ N(0, 1), w BF16
+= 1 + 0.1 N(0, 1), eps = 1e-6.  One step is one non-deterministic backward
+(what the window table runs for deterministic=False) through the C ABI.  The
+same run then times every other configuration the same way and lists them
+under "configs": T = 256, H = 1536; T = 65536, H = 2048 (outlier family, FP32
+weight); the per-head views [32768, 24, 256] (strided) and [32768, 4, 256];
+and the accuracy sweep's shapes H in {4096, 5120} x T in {4096, 44032, 65536,
+131072}.  One JSON line on rank 0.
 
   value         achieved GB/s = algorithmic bytes of the step / its device
                 time (inputs resident in HBM, L2 flushed before every step)
@@ -14,12 +20,18 @@ C ABI.  Printed as one JSON line on rank 0.
   roofline      the main kernel alone, timed with CUDA events on its stream,
                 against the measured HBM copy bandwidth
   cpu_baseline  the FP64 CPU oracle on a bounded sample of the same workload
+  configs       per configuration: deterministic and non-deterministic
+                backward, the main kernel alone (and the forward where the
+                configuration asks for it), each in us, GB/s and as a fraction
+                of the copy peak
 
-``--impl reference`` times the oracle instead (host cores, a bounded sample
-per step) and prints the reference line.  ``--profile`` runs a minimal launch
-sequence for ncu.  Under torchrun each rank runs an independent replica (the
-path has no cross-GPU exchange on one box); value sums the ranks' bytes over
-the slowest rank's time.
+``--workload NAME`` times one workload only.  ``--impl reference`` times the
+oracle instead (host cores, a bounded sample per step) and prints the
+reference line.  ``--profile`` runs a minimal launch sequence for ncu, and
+``--record-traffic`` turns an ncu CSV of that sequence into the DRAM-traffic
+record under profiles/.  Under torchrun each rank runs an independent replica
+(the path has no cross-GPU exchange on one box); value sums the ranks' bytes
+over the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -37,19 +49,46 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "bwd µs & achieved HBM GB/s (fraction of GB300 peak) per (H,T,w dtype,det mode)"
-WORKLOAD = "h2048_t65536_outlier_w32"
+HEADLINE = "h6144_t131072_res"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 ACCUM = {"plain": 0, "blocked": 1, "twosum": 2, "kahan": 3}
+
+# The configurations timed after the headline, with the operations each asks
+# for: T = 256 H = 1536 (forward and both backward modes); T = 65536 H = 2048
+# outlier family with an FP32 weight; the per-head views; the accuracy
+# sweep's widths at each of its T (BF16 weight, and FP32 at T = 65536).
+CONFIGS = (
+    [("h1536_t256", ("fwd", "det", "nondet", "main")),
+     ("h2048_t65536_outlier_w32", ("det", "nondet", "main")),
+     ("heads24_t32768_strided", ("det", "nondet", "main")),
+     ("heads4_t32768", ("det", "nondet", "main"))]
+    + [(f"h{H}_t{T}_sweep", ("det", "nondet", "main")) for H in (4096, 5120) for T in (4096, 44032, 65536, 131072)]
+    + [(f"h{H}_t65536_sweep_w32", ("det", "nondet", "main")) for H in (4096, 5120)]
+)
+
+# The pages' own GB300 latencies for exactly these shapes and weight dtypes
+# (the "Speedups ... GB300 windows" commit quoted on the PR #8208 page, "GB300
+# table": median CUPTI span of a CUDA-graph replay with L2 flushed) -- context
+# only, measured under another protocol on another software stack.
+PAGES_GB300_US = {
+    "h1536_t256": {"fwd": 1.98, "det": 5.76, "nondet": 5.86},
+    "h4096_t4096_sweep": {"det": 23.55, "nondet": 23.65},
+    "h4096_t65536_sweep": {"det": 249.76, "nondet": 257.86},
+    "h5120_t4096_sweep": {"det": 26.85, "nondet": 26.85},
+    "h5120_t65536_sweep": {"det": 314.30, "nondet": 363.10},
+    "h5120_t65536_sweep_w32": {"det": 313.94, "nondet": 369.71},
+}
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--workload", default=None, help="time this workload only (default: the headline + configs)")
+    ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["det", "nondet", "fwd", "main", "all"], default=None,
                     help="run only the named loop(s) with few launches (for ncu); prints per-call times")
@@ -57,6 +96,16 @@ def parse_args(argv=None):
                     help="with --profile: force the per-thread dw accumulation form")
     ap.add_argument("--graph", action="store_true",
                     help="with --profile: time CUDA-graph replays of one call (no host launch cost)")
+    ap.add_argument("--source-hash", action="store_true", help="print the kernel sources' hash and exit")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="record the DRAM bytes per launch of --kernel in an ncu CSV (taken on the sources "
+                         "whose hash --hash gives) into profiles/traffic.json for --workload")
+    ap.add_argument("--kernel", default="bwd_rows_kernel")
+    ap.add_argument("--hash", default=None)
+    ap.add_argument("--summary", default=None, help="with --record-traffic: the profiles/ summary it backs")
+    ap.add_argument("--command", default=None, help="with --record-traffic: the ncu command that made the CSV")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="with --record-traffic: units of the full workload per captured unit")
     return ap.parse_args(argv)
 
 
@@ -105,11 +154,15 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def traffic_json():
+    return os.path.join(ROOT, "profiles", "traffic.json")
+
+
 def traffic_record(kernel: str, workload: str):
     """The committed ncu record (DRAM bytes per launch, the summary file) when
-    it holds for the current kernel sources; else None."""
+    its counters were taken on the current kernel sources; else None."""
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        with open(traffic_json()) as f:
             rec = json.load(f)
     except Exception:
         return None
@@ -120,10 +173,69 @@ def traffic_record(kernel: str, workload: str):
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary when it was taken
-    on the current kernel sources; else None."""
     ent = traffic_record(kernel, workload)
     return ent.get("dram_bytes_per_launch") if ent else None
+
+
+_UNITS = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
+          "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0}
+
+
+def parse_ncu_csv(path: str, kernel: str):
+    """Per-launch metric values (base units) of the launches of `kernel` in an
+    ncu --csv --metrics log."""
+    import csv
+
+    launches = {}
+    with open(path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        name = row.get("Kernel Name", "")
+        if kernel not in name:
+            continue
+        unit = (row.get("Metric Unit") or "").strip().lower()
+        try:
+            val = float(row["Metric Value"].replace(",", ""))
+        except (KeyError, ValueError):
+            continue
+        launches.setdefault(row["ID"], {})[row["Metric Name"]] = val * _UNITS.get(unit, 1.0)
+    return [launches[k] for k in sorted(launches, key=int)]
+
+
+def record_traffic(args):
+    """Write profiles/traffic.json's entry for (kernel, workload) from an ncu
+    CSV.  The entry carries the hash of the sources the counters were taken on
+    (the hash the box printed before the capture), and is refused unless that
+    is the hash of the sources here: counters are never carried over to code
+    they were not taken on."""
+    if not args.workload:
+        raise SystemExit("--record-traffic needs --workload")
+    here = kernel_source_hash()
+    if args.hash != here:
+        raise SystemExit(f"counters taken on sources {args.hash}, but the sources here hash to {here}")
+    ls = parse_ncu_csv(args.record_traffic, args.kernel)
+    if not ls:
+        raise SystemExit(f"no launch of {args.kernel} in {args.record_traffic}")
+    per = [d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"] for d in ls]
+    dur = [d.get("gpu__time_duration.sum") for d in ls if d.get("gpu__time_duration.sum")]
+    try:
+        with open(traffic_json()) as f:
+            rec = json.load(f)
+    except Exception:
+        rec = {}
+    rec[f"{args.kernel}:{args.workload}"] = {
+        "source_hash": here,
+        "dram_bytes_per_launch": int(round(statistics.mean(per) * args.scale)),
+        "launches": len(per),
+        "ncu_us_per_launch": round(statistics.mean(dur) * 1e6 * args.scale, 2) if dur else None,
+        "scaled_from_capture": args.scale if args.scale != 1.0 else None,
+        "command": args.command,
+        "summary": args.summary,
+    }
+    with open(traffic_json(), "w") as f:
+        json.dump(rec, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(rec[f"{args.kernel}:{args.workload}"]))
 
 
 class ClockSampler:
@@ -184,46 +296,6 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm)}
-
-
-def make_step_fns(cake, torch, case, dev, accum=None):
-    """Forward / backward callables for one workload, outputs preallocated."""
-    x, dy, w, eps = case["x"], case["dy"], case["w"], case["eps"]
-    res = case.get("residual")
-    dh = case.get("dh")
-    out = cake.cake_rmsnorm_fwd(x, w, eps, residual=res)
-    y, rstd = out[0], out[1]
-    hn = out[2] if res is not None else None
-    h = hn if res is not None else x
-    ws = cake.cake_rmsnorm_bwd_workspace(h, w.dtype, deterministic=False)
-    dx = torch.empty(h.shape, dtype=torch.bfloat16, device=dev)
-    dw = torch.empty(h.shape[-1], dtype=torch.float32, device=dev)
-
-    def bwd(det):
-        if accum is None:
-            return lambda: cake.cake_rmsnorm_bwd(dy, h, rstd, w, dh, deterministic=det, workspace=ws, dx=dx, dw=dw)
-        return lambda: cake.cake_rmsnorm_bwd_forced(dy, h, rstd, w, dh, deterministic=det, force_single=int(not det),
-                                                   force_accum=accum, workspace=ws, dx=dx, dw=dw)
-
-    def forced(form):
-        return lambda: cake.cake_rmsnorm_bwd_forced(dy, h, rstd, w, dh, deterministic=form != 1, force_single=form,
-                                                   force_accum=accum, workspace=ws, dx=dx, dw=dw)
-
-    def fwd():
-        return cake.cake_rmsnorm_fwd(x, w, eps, residual=res, y=y, rstd=rstd, h_new=hn)
-
-    return {
-        "fwd": fwd,
-        "det": bwd(True),
-        "nondet": bwd(False),
-        "single_atomic": forced(1),
-        "single_grid": forced(3),
-        # the checkpointed step of the pages' GB300 tables: forward, forward
-        # recompute, deterministic backward
-        "ckpt": lambda: (fwd(), fwd(), bwd(True)()),
-        "main": lambda: cake.cake_rmsnorm_bwd_main(dy, h, rstd, w, dh, workspace=ws, dx=dx, dw=dw, force_accum=accum),
-        "h": h, "rstd": rstd, "ws": ws, "dx": dx, "dw": dw,
-    }
 
 
 def aggregate_times(times, world, device):
@@ -299,6 +371,141 @@ def describe(spec) -> str:
     return f"[T,{spec['heads']},256] {view}, x 3+N(0,1), dy N(0,1); shared {wd}[256]; eps 1e-6"
 
 
+class Workload:
+    """One workload's device tensors, preallocated outputs and step callables.
+
+    Each step callable comes with the number of library kernels it launches
+    and its algorithmic bytes."""
+
+    def __init__(self, cake, torch, name, dev, seed=0, accum=None):
+        import cake_inputs
+
+        self.name, self.spec = name, cake_inputs.WORKLOADS[name]
+        case = cake_inputs.make(name, seed=seed, device=dev)
+        self.case = case
+        x, dy, w, eps = case["x"], case["dy"], case["w"], case["eps"]
+        res, dh = case.get("residual"), case.get("dh")
+        out = cake.cake_rmsnorm_fwd(x, w, eps, residual=res)
+        y, rstd = out[0], out[1]
+        hn = out[2] if res is not None else None
+        h = hn if res is not None else x
+        ws = cake.cake_rmsnorm_bwd_workspace(h, w.dtype, deterministic=False)
+        dx = torch.empty(h.shape, dtype=torch.bfloat16, device=dev)
+        dw = torch.empty(h.shape[-1], dtype=torch.float32, device=dev)
+        self.x, self.dy, self.w, self.res, self.dh, self.h, self.rstd = x, dy, w, res, dh, h, rstd
+        self.ws, self.dx, self.dw, self.y, self.hn = ws, dx, dw, y, hn
+        self.T = x.shape[0]
+        self.nh = x.shape[1] if x.dim() == 3 else 1
+        self.H = x.shape[-1]
+        self.R = self.T * self.nh
+        wb = w.numel() * w.element_size()
+
+        def variant(det, has_dh, force_single=None):
+            return cake.cake_rmsnorm_bwd_select((self.T, self.nh, self.H), w.dtype, deterministic=det,
+                                                has_dh=has_dh, force_single=force_single,
+                                                force_accum=None if accum is None else ACCUM[accum])
+
+        def bwd(det, ddh):
+            acc = None if accum is None else ACCUM[accum]
+            if acc is None:
+                return lambda: cake.cake_rmsnorm_bwd(dy, h, rstd, w, ddh, deterministic=det, workspace=ws, dx=dx,
+                                                     dw=dw)
+            return lambda: cake.cake_rmsnorm_bwd_forced(dy, h, rstd, w, ddh, deterministic=det, force_single=0,
+                                                       force_accum=acc, workspace=ws, dx=dx, dw=dw)
+
+        def forced(form, ddh):
+            return lambda: cake.cake_rmsnorm_bwd_forced(dy, h, rstd, w, ddh, deterministic=form != 1,
+                                                       force_single=form, workspace=ws, dx=dx, dw=dw)
+
+        def fwd():
+            return cake.cake_rmsnorm_fwd(x, w, eps, residual=res, y=y, rstd=rstd, h_new=hn)
+
+        self.steps = {}
+        for suffix, ddh in (("", dh), ("_nodh", None)):
+            if suffix and dh is None:
+                continue
+            vd, vn = variant(True, ddh is not None), variant(False, ddh is not None)
+            nb = workload_bytes(self.R, self.H, wb, vd["ctas"], dh=ddh is not None)
+            nd_pair = vn["single"] == 0
+            self.steps["det" + suffix] = (bwd(True, ddh), 2, nb["pair"], vd)
+            self.steps["nondet" + suffix] = (bwd(False, ddh), 2 if nd_pair else 1,
+                                             nb["pair"] if nd_pair else nb["single"], vn)
+            self.steps["main" + suffix] = (
+                (lambda ddh=ddh: cake.cake_rmsnorm_bwd_main(dy, h, rstd, w, ddh, workspace=ws, dx=dx, dw=dw,
+                                                            force_accum=None if accum is None else ACCUM[accum])),
+                1, nb["main"], vd)
+            if not suffix:
+                va = variant(False, ddh is not None, 1)
+                vg = variant(True, ddh is not None, 3)
+                self.steps["single_atomic"] = (forced(1, ddh), 1, nb["single"], va)
+                self.steps["single_grid"] = (forced(3, ddh), 1,
+                                             workload_bytes(self.R, self.H, wb, vg["ctas"], dh=ddh is not None)["pair"],
+                                             vg)
+                fb = workload_bytes(self.R, self.H, wb, 0, res=res is not None)["fwd"]
+                self.steps["fwd"] = (fwd, 1, fb, None)
+                # the checkpointed step of the pages' GB300 tables: forward,
+                # forward recompute, deterministic backward
+                self.steps["ckpt_2xfwd_bwd"] = (lambda: (fwd(), fwd(), bwd(True, ddh)()), 4, 2 * fb + nb["pair"], vd)
+
+
+def time_modes(torch, wl: Workload, modes, K, Wm, flush, stream, world, dev, peak):
+    """Time the listed step kinds of one workload; per mode us, GB/s and the
+    fraction of the copy peak (GB/s per GPU), plus the launch count."""
+    out, launches = {}, 0
+    for m in modes:
+        fn, nl, nbytes, _ = wl.steps[m]
+        times = time_loop(torch, fn, K, Wm, flush, stream)
+        tot, mean = aggregate_times(times, world, dev)
+        gbs = replica_gbs(nbytes, K, world, tot)
+        out[m] = {"us": round(mean * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / world / peak, 4),
+                  "bytes": nbytes}
+        launches += nl * K
+    return out, launches
+
+
+def short_variant(v):
+    if not v:
+        return None
+    return {k: v[k] for k in ("single", "dw_accum", "vec_per_thread", "warps_per_row", "row_groups",
+                              "rows_per_group", "stages", "ctas")}
+
+
+def e2e_loop(cake, torch, wl: Workload, K, Wm, flush, stream, dev, det):
+    """The backward through the public entry point from pinned host buffers:
+    every step copies its inputs in and dx, dw out (all inside the timed region)."""
+    def host(t):
+        if t is None:
+            return None
+        if not t.is_contiguous():  # a strided view travels as its whole buffer
+            t = t.as_strided((t.untyped_storage().nbytes() // t.element_size(),), (1,), 0)
+        return t.cpu().pin_memory()
+
+    h, dy, dh, rstd, w, dx = wl.h, wl.dy, wl.dh, wl.rstd, wl.w, wl.dx
+    hx, hdy, hdh, hrstd, hw = (host(t) for t in (h, dy, dh, rstd, w))
+    hdx = torch.empty(dx.shape, dtype=torch.bfloat16).pin_memory()
+    hdw = torch.empty(wl.H, dtype=torch.float32).pin_memory()
+    bx = torch.empty(hx.shape, dtype=hx.dtype, device=dev)
+    x2 = bx if h.is_contiguous() else bx.as_strided(h.shape, h.stride(), h.storage_offset())
+    dy2, r2, w2, dx2 = (torch.empty_like(t) for t in (dy, rstd, w, dx))
+    dh2 = torch.empty_like(dh) if dh is not None else None
+
+    def step():
+        bx.copy_(hx, non_blocking=True)
+        dy2.copy_(hdy, non_blocking=True)
+        if dh2 is not None:
+            dh2.copy_(hdh, non_blocking=True)
+        r2.copy_(hrstd, non_blocking=True)
+        w2.copy_(hw, non_blocking=True)
+        cake.cake_rmsnorm_bwd(dy2, x2, r2, w2, dh2, deterministic=det, workspace=wl.ws, dx=dx2, dw=wl.dw)
+        hdx.copy_(dx2, non_blocking=True)
+        hdw.copy_(wl.dw, non_blocking=True)
+
+    times = time_loop(torch, step, K, Wm, flush, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hdy, hdh, hrstd, hw) if t is not None)
+    d2h = hdx.numel() * 2 + hdw.numel() * 4
+    return times, h2d, d2h
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -315,89 +522,54 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     import bwd_dw_column_gb300 as cake
-    import cake_inputs
 
-    spec = cake_inputs.WORKLOADS[args.workload]
-    case = cake_inputs.make(args.workload, seed=rank, device=dev)
-    x, dy, w = case["x"], case["dy"], case["w"]
-    dh, res = case.get("dh"), case.get("residual")
-    fns = make_step_fns(cake, torch, case, dev)
-    h, rstd, ws, dx, dw = fns["h"], fns["rstd"], fns["ws"], fns["dx"], fns["dw"]
-    T = x.shape[0]
-    nh = x.shape[1] if x.dim() == 3 else 1
-    H = x.shape[-1]
-    R = T * nh
-    variant = cake.cake_rmsnorm_bwd_select((T, nh, H), w.dtype, deterministic=True, has_dh=dh is not None)
-    nd_variant = cake.cake_rmsnorm_bwd_select((T, nh, H), w.dtype, deterministic=False, has_dh=dh is not None)
-    nbytes = workload_bytes(R, H, w.numel() * w.element_size(), variant["ctas"], dh=dh is not None,
-                            res=res is not None)
+    head = args.workload or HEADLINE
+    configs = [] if (args.no_configs or args.workload) else CONFIGS
+    peak, peak_kind = measured_peak()
     flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
     K, Wm = args.steps, max(3, args.warmup)
 
+    wl = Workload(cake, torch, head, dev, seed=rank)
+    has_dh = wl.dh is not None
+    head_modes = ["nondet", "det", "main", "fwd", "single_atomic", "single_grid", "ckpt_2xfwd_bwd"]
+    if has_dh:
+        head_modes += ["nondet_nodh", "det_nodh", "main_nodh"]
+
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    entries = []
     with ClockSampler(local) as clk:
-        t_det = time_loop(torch, fns["det"], K, Wm, flush, stream)
-        t_main = time_loop(torch, fns["main"], K, Wm, flush, stream)
-        t_nd = time_loop(torch, fns["nondet"], K, Wm, flush, stream)
-        t_sa = time_loop(torch, fns["single_atomic"], K, Wm, flush, stream)
-        t_sg = time_loop(torch, fns["single_grid"], K, Wm, flush, stream)
-        t_fwd = time_loop(torch, fns["fwd"], K, Wm, flush, stream)
-        t_ck = time_loop(torch, fns["ckpt"], K, Wm, flush, stream)
+        modes, launches = time_modes(torch, wl, head_modes, K, Wm, flush, stream, world, dev, peak)
+        for name, ms in configs:
+            cw = Workload(cake, torch, name, dev, seed=rank)
+            cm, cl = time_modes(torch, cw, ms, K, Wm, flush, stream, world, dev, peak)
+            launches += cl
+            ent = {"workload": name, "T": cw.T, "heads": cw.nh, "H": cw.H,
+                   "w_dtype": "fp32" if cw.w.dtype == torch.float32 else "bf16", "inputs": describe(cw.spec),
+                   "modes": cm, "variant": short_variant(cw.steps["det"][3]),
+                   "main_kernel_frac": cm["main"]["frac"],
+                   "traffic": recorded_traffic("bwd_rows_kernel", name),
+                   "traffic_summary": (traffic_record("bwd_rows_kernel", name) or {}).get("summary")}
+            if cw.R >= 32768 and cw.T >= 32768:
+                ent["at_least_75pct_both_modes"] = bool(cm["det"]["frac"] >= 0.75 and cm["nondet"]["frac"] >= 0.75)
+            if name in PAGES_GB300_US:
+                ent["pages_gb300_us"] = PAGES_GB300_US[name]
+            entries.append(ent)
+            del cw
+            torch.cuda.empty_cache()
     torch.cuda.synchronize()
     clocks = clk.summary()
 
-    # end to end through the C ABI from pinned host buffers: every step copies
-    # the backward's inputs in and dx, dw out
-    def host(t):
-        if t is None:
-            return None
-        if not t.is_contiguous():  # a strided view travels as its whole buffer
-            t = t.as_strided((t.untyped_storage().nbytes() // t.element_size(),), (1,), 0)
-        return t.cpu().pin_memory()
-
-    hx, hdy, hdh, hrstd, hw = (host(t) for t in (h, dy, dh, rstd, w))
-    hdx = torch.empty(dx.shape, dtype=torch.bfloat16).pin_memory()
-    hdw = torch.empty(H, dtype=torch.float32).pin_memory()
-    bx = torch.empty(hx.shape, dtype=hx.dtype, device=dev)
-    x2 = bx if h.is_contiguous() else bx.as_strided(h.shape, h.stride(), h.storage_offset())
-    dy2, r2, w2, dx2 = (torch.empty_like(t) for t in (dy, rstd, w, dx))
-    dh2 = torch.empty_like(dh) if dh is not None else None
-
-    def e2e_step():
-        bx.copy_(hx, non_blocking=True)
-        dy2.copy_(hdy, non_blocking=True)
-        if dh2 is not None:
-            dh2.copy_(hdh, non_blocking=True)
-        r2.copy_(hrstd, non_blocking=True)
-        w2.copy_(hw, non_blocking=True)
-        cake.cake_rmsnorm_bwd(dy2, x2, r2, w2, dh2, deterministic=True, workspace=ws, dx=dx2, dw=dw)
-        hdx.copy_(dx2, non_blocking=True)
-        hdw.copy_(dw, non_blocking=True)
-
-    t_e2e = time_loop(torch, e2e_step, K, Wm, flush, stream)
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hdy, hdh, hrstd, hw) if t is not None)
-    d2h = hdx.numel() * 2 + hdw.numel() * 4
+    t_e2e, h2d, d2h = e2e_loop(cake, torch, wl, K, Wm, flush, stream, dev, det=False)
+    launches += 2 * K
     assert cake.cake_rmsnorm_device_status() == 0
-
-    agg = lambda times: aggregate_times(times, world, dev)
-
-    tot_det, mean_det = agg(t_det)
-    tot_main, mean_main = agg(t_main)
-    tot_nd, mean_nd = agg(t_nd)
-    tot_sa, mean_sa = agg(t_sa)
-    tot_sg, mean_sg = agg(t_sg)
-    nd_bytes = nbytes["pair"] if nd_variant["single"] == 0 else nbytes["single"]
-    tot_fwd, mean_fwd = agg(t_fwd)
-    tot_ck, mean_ck = agg(t_ck)
-    tot_e2e, mean_e2e = agg(t_e2e)
-    gbs = lambda b, tot_ms: replica_gbs(b, K, world, tot_ms)
+    tot_e2e, mean_e2e = aggregate_times(t_e2e, world, dev)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and spec["kind"] == "plain":
-        cpu = oracle_baseline(case, T, H, budget_s=10.0)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl.spec["kind"] in ("plain", "res"):
+        cpu = oracle_baseline(wl.case, wl.T, wl.H, budget_s=10.0)
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -405,17 +577,17 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = measured_peak()
-    achieved_main = nbytes["main"] / (mean_main * 1e-3) / 1e9
-    value = gbs(nbytes["pair"], tot_det)
+    nd = modes["nondet"]
+    main = modes["main"]
+    nd_variant = wl.steps["nondet"][3]
     line = {
         "metric": METRIC,
-        "value": round(value, 1),
+        "value": nd["GB/s"],
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
         "warmup": Wm,
-        "ms_per_step": round(mean_det, 5),
+        "ms_per_step": round(nd["us"] / 1e3, 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -423,63 +595,43 @@ def run_ours(args):
         "data": "synthetic",
         "impl": "ours",
         "config": {
-            "workload": args.workload,
-            "T": T, "heads": nh, "H": H, "w_dtype": "fp32" if w.dtype == torch.float32 else "bf16",
-            "inputs": describe(spec),
-            "mode": "deterministic (main + fixed-order reduce)",
+            "workload": head,
+            "T": wl.T, "heads": wl.nh, "H": wl.H, "w_dtype": "fp32" if wl.w.dtype == torch.float32 else "bf16",
+            "inputs": describe(wl.spec),
+            "mode": "non-deterministic backward (the window table's choice for deterministic=False)"
+                    + (", with the gradient dh reaching h_new" if has_dh else ""),
             "io_dtype": "bf16 activations, fp32 rstd/dw",
             "l2": "flushed before every timed step (256 MiB write, then 256 MiB read so no dirty line is left)",
             "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
-            "variant": variant,
+            "variant": short_variant(nd_variant),
         },
-        "bwd_us": round(mean_det * 1e3, 2),
-        "bytes_per_step": nbytes["pair"],
-        "frac_of_peak": round(value / world / peak, 4),
-        "modes": {
-            "det_pair": {"us": round(mean_det * 1e3, 2), "GB/s": round(gbs(nbytes["pair"], tot_det), 1),
-                         "bytes": nbytes["pair"]},
-            "det_main_kernel": {"us": round(mean_main * 1e3, 2), "GB/s": round(achieved_main, 1),
-                                "bytes": nbytes["main"]},
-            "nondet": {"us": round(mean_nd * 1e3, 2), "GB/s": round(gbs(nd_bytes, tot_nd), 1),
-                       "bytes": nd_bytes, "variant": nd_variant},
-            # the single-kernel forms the non-deterministic mode may run
-            # (the table picks the pair, which is faster at every measured
-            # shape): FP64 L2 atomics, and the cooperative grid form
-            "single_atomic": {"us": round(mean_sa * 1e3, 2), "GB/s": round(gbs(nbytes["single"], tot_sa), 1),
-                              "bytes": nbytes["single"]},
-            "single_grid": {"us": round(mean_sg * 1e3, 2), "GB/s": round(gbs(nbytes["pair"], tot_sg), 1),
-                            "bytes": nbytes["pair"]},
-            "fwd": {"us": round(mean_fwd * 1e3, 2), "GB/s": round(gbs(nbytes["fwd"], tot_fwd), 1),
-                    "bytes": nbytes["fwd"]},
-            "ckpt_2xfwd_bwd": {"us": round(mean_ck * 1e3, 2),
-                               "GB/s": round(gbs(2 * nbytes["fwd"] + nbytes["pair"], tot_ck), 1),
-                               "bytes": 2 * nbytes["fwd"] + nbytes["pair"]},
-        },
+        "bwd_us": nd["us"],
+        "bytes_per_step": nd["bytes"],
+        "frac_of_peak": nd["frac"],
+        "modes": modes,
         "roofline": {
             "bound": "hbm",
-            "kernel": "bwd_rows_kernel (main kernel of the deterministic pair)",
-            "achieved": round(achieved_main, 1),
+            "kernel": "bwd_rows_kernel (main kernel of the backward pair)",
+            "achieved": round(main["GB/s"] / world, 1),
             "peak": peak,
             "peak_kind": peak_kind,
             "unit": "GB/s",
-            "frac": round(achieved_main / peak, 4),
-            "traffic": recorded_traffic("bwd_rows_kernel", args.workload),
-            "traffic_summary": (traffic_record("bwd_rows_kernel", args.workload) or {}).get("summary"),
-            "algorithmic_bytes": nbytes["main"],
+            "frac": main["frac"],
+            "traffic": recorded_traffic("bwd_rows_kernel", head),
+            "traffic_summary": (traffic_record("bwd_rows_kernel", head) or {}).get("summary"),
+            "algorithmic_bytes": main["bytes"],
         },
         "e2e": {
-            "value": round(gbs(nbytes["pair"], tot_e2e), 1),
+            "value": round(replica_gbs(nd["bytes"], K, world, tot_e2e), 1),
             "unit": "GB/s",
             "ms_per_step": round(mean_e2e, 4),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
         },
-        "gpu_launches": K * (2 + 1 + (1 if nd_variant["single"] else 2) + 1 + 1 + 1 + 4 + 2),
-        "gpu_launches_detail": {"det": 2 * K, "main_only": K, "nondet": K * (1 if nd_variant["single"] else 2),
-                                "single_atomic": K, "single_grid": K, "fwd": K, "ckpt_2xfwd_bwd": 4 * K,
-                                "e2e": 2 * K},
+        "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "configs": entries,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -494,50 +646,59 @@ def run_profile(args):
     import __graft_entry__
     __graft_entry__.build()
     import bwd_dw_column_gb300 as cake
-    import cake_inputs
 
     dev = torch.device("cuda", 0)
-    case = cake_inputs.make(args.workload, seed=0, device=dev)
-    fns = make_step_fns(cake, torch, case, dev, ACCUM.get(args.accum) if args.accum else None)
+    wl = Workload(cake, torch, args.workload or HEADLINE, dev, accum=args.accum)
     names = ["fwd", "det", "nondet"] if args.profile == "all" else [args.profile]
     out = {}
     stream = torch.cuda.current_stream()
     for n in names:
-        fn = fns[n]
+        fn = wl.steps[n][0]
         if args.graph:
             fn()  # first call on the device: attributes and addresses set up before capture
             torch.cuda.synchronize()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
-                fns[n]()
+                wl.steps[n][0]()
             fn = graph.replay
         ts = [t * 1e3 for t in time_loop(torch, fn, args.steps, args.warmup, None, stream)]
         out[n] = {"us_median": round(statistics.median(ts), 2), "us_min": round(min(ts), 2)}
     assert cake.cake_rmsnorm_device_status() == 0
-    print(json.dumps({"profile": args.workload, "accum": args.accum, "us_per_call": out}), flush=True)
+    print(json.dumps({"profile": wl.name, "accum": args.accum, "us_per_call": out,
+                      "source_hash": kernel_source_hash()}), flush=True)
 
 
 # ------------------------------------------------------------ the oracle
 
 def oracle_sample(case, H, rows):
     """Seconds the oracle's backward takes on the first `rows` rows (dx of
-    those rows and dw over them), its rstd input prepared outside the timing."""
+    those rows and dw over them), its inputs (rstd; h_new on the residual
+    route) prepared outside the timing."""
     import numpy as np
     import torch
 
     import oracle
 
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     x = case["x"][:rows].cpu()
     dy = case["dy"][:rows].cpu()
     w = case["w"].cpu()
-    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     xv, dyv = oracle.View.contiguous(bits(x)), oracle.View.contiguous(bits(dy))
     wb = w.numpy() if w.dtype == torch.float32 else bits(w)
-    _, r64, _ = oracle.fwd_rows(rows, 1, H, xv, wb, case["eps"], want_y=False, want_h=False)
+    res = case.get("residual")
+    if res is not None:
+        rv = oracle.View.contiguous(bits(res[:rows].cpu()))
+        _, r64, hn = oracle.fwd_rows(rows, 1, H, xv, wb, case["eps"], residual=rv, want_y=False, want_h=True)
+        hv = oracle.View.contiguous(hn)
+    else:
+        _, r64, _ = oracle.fwd_rows(rows, 1, H, xv, wb, case["eps"], want_y=False, want_h=False)
+        hv = xv
+    dh = case.get("dh")
+    dhv = oracle.View.contiguous(bits(dh[:rows].cpu())) if dh is not None else None
     rin = r64.astype(np.float32)
     t0 = time.perf_counter()
-    oracle.bwd_rows(rows, 1, H, dyv, xv, rin, wb)
-    oracle.dw_cols(rows, 1, H, dyv, xv, rin)
+    oracle.bwd_rows(rows, 1, H, dyv, hv, rin, wb, dh=dhv)
+    oracle.dw_cols(rows, 1, H, dyv, hv, rin)
     return time.perf_counter() - t0
 
 
@@ -554,18 +715,19 @@ def cpu_model():
 
 def oracle_baseline(case, T, H, budget_s=10.0):
     """The oracle on a bounded sample (the leading rows) sized to ~budget_s."""
-    probe = min(T, 1024)
+    probe = min(T, 256)
     dt = oracle_sample(case, H, probe)
     rows = int(min(T, max(probe, probe * budget_s / max(dt, 1e-6))))
     dt = oracle_sample(case, H, rows)
-    b = workload_bytes(rows, H, case["w"].numel() * case["w"].element_size(), 0)["rows_only"]
+    b = workload_bytes(rows, H, case["w"].numel() * case["w"].element_size(), 0,
+                       dh=case.get("dh") is not None)["rows_only"]
     return {
         "value": round(b / dt / 1e9, 4),
         "unit": "GB/s",
         "cores": 1,
         "kind": "oracle",
-        "sample": f"FP64 C oracle backward (dx and dw) on the first {rows} of {T} rows of the workload, "
-                  f"{dt:.2f} s, single thread",
+        "sample": f"FP64 C oracle backward (dx and dw{', with dh' if case.get('dh') is not None else ''}) on the "
+                  f"first {rows} of {T} rows of the workload, {dt:.2f} s, single thread",
         "cpu": cpu_model(),
         "host_cores": os.cpu_count(),
     }
@@ -578,21 +740,28 @@ def run_reference(args):
     import cake_inputs
     import oracle
     oracle.build()
-    spec = cake_inputs.WORKLOADS[args.workload]
+    name = args.workload or HEADLINE
+    spec = cake_inputs.WORKLOADS[name]
+    if spec["kind"] not in ("plain", "res"):
+        raise SystemExit("the reference arm times plain and residual workloads")
     T, H = spec["T"], spec["H"]
-    case = cake_inputs.make(args.workload, seed=0, device="cpu")
+    # only the sampled leading rows are ever read: draw a prefix of the
+    # workload's rows (the same generator sequence as the full workload for
+    # row-wise draws)
     K, Wm = args.steps, max(3, args.warmup)
-    # size each step so the whole run stays within about two minutes
-    probe = min(T, 512)
+    case = cake_inputs.make(name, seed=0, device="cpu", **({"T": min(T, 4096)} if spec["kind"] == "res" else {}))
+    probe = min(T, 128)
     dt = oracle_sample(case, H, probe)
     per_step_s = min(10.0, 120.0 / (K + Wm))
-    rows = int(min(T, max(64, probe * per_step_s / max(dt, 1e-6))))
+    rows = int(min(case["x"].shape[0], max(16, probe * per_step_s / max(dt, 1e-6))))
     for _ in range(Wm):
         oracle_sample(case, H, rows)
     times = [oracle_sample(case, H, rows) for _ in range(K)]
-    b = workload_bytes(rows, H, case["w"].numel() * case["w"].element_size(), 0)["rows_only"]
+    b = workload_bytes(rows, H, case["w"].numel() * case["w"].element_size(), 0,
+                       dh=case.get("dh") is not None)["rows_only"]
     value = K * b / sum(times) / 1e9
-    sample = f"FP64 C oracle backward (dx and dw) on the first {rows} of {T} rows per step, single thread"
+    sample = (f"FP64 C oracle backward (dx and dw{', with dh' if case.get('dh') is not None else ''}) on "
+              f"{rows} rows of the {T}-row workload per step, single thread")
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -607,7 +776,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "T": T, "H": H, "rows_per_step": rows},
+        "config": {"workload": name, "T": T, "H": H, "rows_per_step": rows},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
                          "cpu": cpu_model(), "host_cores": os.cpu_count()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -618,7 +787,11 @@ def run_reference(args):
 
 def main():
     args = parse_args()
-    if args.profile:
+    if args.source_hash:
+        print(kernel_source_hash())
+    elif args.record_traffic:
+        record_traffic(args)
+    elif args.profile:
         run_profile(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -31,7 +31,8 @@ import torch
 __all__ = [
     "CakeError", "load_library", "cake_rmsnorm_fwd", "cake_rmsnorm_bwd", "cake_rmsnorm_bwd_forced",
     "cake_rmsnorm_bwd_main", "cake_rmsnorm_bwd_reduce", "cake_rmsnorm_bwd_noalloc",
-    "cake_rmsnorm_bwd_workspace_size", "cake_rmsnorm_bwd_workspace", "cake_rmsnorm_bwd_select",
+    "cake_rmsnorm_bwd_workspace_size", "cake_rmsnorm_bwd_workspace", "cake_rmsnorm_bwd_workspace_init",
+    "cake_rmsnorm_bwd_select", "cake_rmsnorm_bwd_timeout_test",
     "cake_rmsnorm_device_status", "cake_status_str", "cake_rmsnorm_plan_occupancy", "LIB_PATH", "DW_PLAIN", "DW_BLOCKED", "DW_TWOSUM", "DW_KAHAN",
 ]
 
@@ -105,6 +106,9 @@ def load_library(path: str = LIB_PATH):
         lib.cake_rmsnorm_bwd_noalloc.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_noalloc.argtypes = [_P(_Shape), _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_int,
                                                  _P(_Tensor), _P(_Tensor), _vp, _vp]
+        lib.cake_rmsnorm_bwd_timeout_test.restype = ctypes.c_int
+        lib.cake_rmsnorm_bwd_timeout_test.argtypes = [_P(_Shape), _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_int,
+                                                      _P(_Tensor), _vp, _vp, ctypes.c_size_t, ctypes.c_uint32, _vp]
         lib.cake_rmsnorm_bwd_select.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_select.argtypes = [_P(_Shape), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, _P(_Variant)]
@@ -342,6 +346,37 @@ def cake_rmsnorm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, rstd: torch.Tens
                                       ctypes.byref(_tensor(dx)), ctypes.c_void_p(dw.data_ptr()), _stream(stream))
     _check(st, "cake_rmsnorm_bwd_noalloc")
     return dx, dw
+
+
+def cake_rmsnorm_bwd_timeout_test(dy: torch.Tensor, x: torch.Tensor, rstd: torch.Tensor, w: torch.Tensor, *,
+                                  workspace: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor,
+                                  wait_limit_us: int = 2000, stream=None):
+    """Run the grid form with a barrier that cannot complete, so that its bounded
+    wait runs out after ``wait_limit_us`` (tests of the timeout path).  Afterwards
+    the device status reads CAKE_ERR_TIMEOUT and ``workspace`` needs
+    re-initialising."""
+    lib = load_library()
+    _need_cuda(dy, x, rstd, w, workspace, dx, dw)
+    _same_rows(x, dy, "dy")
+    _same_rows(x, dx, "dx")
+    shape = _shape(x)
+    st = lib.cake_rmsnorm_bwd_timeout_test(ctypes.byref(shape), ctypes.byref(_tensor(dy)), ctypes.byref(_tensor(x)),
+                                           ctypes.c_void_p(rstd.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                                           _w_dtype(w), ctypes.byref(_tensor(dx)), ctypes.c_void_p(dw.data_ptr()),
+                                           ctypes.c_void_p(workspace.data_ptr()),
+                                           workspace.numel() * workspace.element_size(), int(wait_limit_us),
+                                           _stream(stream))
+    _check(st, "cake_rmsnorm_bwd_timeout_test")
+
+
+def cake_rmsnorm_bwd_workspace_init(workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """Zero a workspace (an asynchronous memset on the stream)."""
+    lib = load_library()
+    _need_cuda(workspace)
+    st = lib.cake_rmsnorm_bwd_workspace_init(ctypes.c_void_p(workspace.data_ptr()),
+                                             workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "cake_rmsnorm_bwd_workspace_init")
+    return workspace
 
 
 def cake_rmsnorm_bwd_select(shape, w_dtype=torch.bfloat16, deterministic=True, has_dh=False,

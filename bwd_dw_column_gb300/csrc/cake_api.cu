@@ -129,10 +129,43 @@ static RowLayout row_layout(int H, Kind kind)
     const int nvec = H / 8;
     if (nvec <= 32)
         return {1, 1};
-    // backward, 4096 < H <= 5376: 24 columns per thread on 6 or 7 warps,
-    // which leaves room for a second row group or a second CTA per SM
-    // (GB300, T = 65536: H = 4608 det 5 %, H = 4864 3 %, H = 5120 10 % faster
-    // than 8 columns per thread on 18 - 20 warps)
+    // backward, 24 or 32 columns per thread where the row splits into W warps
+    // with W dividing 12 and enough of the lanes' vectors in use: an SM then
+    // holds 12 consumer warps as 12 / W row groups (or, W = 1, as three CTAs
+    // of four groups), so each thread's per-row work -- the row sums, their
+    // barrier, the rstd and the dx scale -- is shared by 24 or 32 columns
+    // instead of 8.  "Enough" is 3/4, or 7/8 where 8 columns per thread
+    // still fit four row groups in a CTA (W <= 6): a row's time is that of
+    // its busiest warp, so idle lanes cost their share of the bytes.  The
+    // wider vector wins a tie.  GB300, T = 65536, deterministic pair against
+    // 8 columns per thread: H = 768 0.85 vs 0.77 of the copy peak, 1024 0.86
+    // vs 0.81, 1792 0.86 vs 0.84, 2048 0.91 vs 0.87, 2304 0.91 vs 0.77, 2560
+    // 0.90 vs 0.80, 3072 0.93 vs 0.88, 3584 0.90 vs 0.80, 4096 0.94 vs 0.88,
+    // 4608 0.93 vs 0.92, 5376 0.92 vs 0.80, 6144 0.96 vs 0.84; H = 1152 and
+    // 1280 (3/4 and 5/6 of the lanes at 24 columns) ran 0.69 and 0.78 against
+    // 0.76 and 0.85, hence the 7/8.
+    if (kind == kBwd) {
+        const int w8 = (nvec + 31) / 32;
+        const int need_num = w8 <= 6 ? 7 : 3, need_den = w8 <= 6 ? 8 : 4;
+        RowLayout best{0, 0};
+        int best_used = 0, best_slots = 1;
+        for (int vpt = 4; vpt >= 3; --vpt) {
+            const RowLayout l = layout_for(H, vpt);
+            const int slots = 32 * vpt * l.W;
+            if (12 % l.W != 0 || need_den * nvec < need_num * slots)
+                continue;
+            if ((int64_t)nvec * best_slots > (int64_t)best_used * slots) {
+                best = l;
+                best_used = nvec;
+                best_slots = slots;
+            }
+        }
+        if (best.vpt)
+            return best;
+    }
+    // backward, 4096 < H <= 5376 outside the rule above: 24 columns per
+    // thread on 7 warps, two CTAs per SM (GB300, T = 65536: H = 5120 0.93 of
+    // the copy peak, against 0.89 with 32 columns on 5 warps)
     if (kind == kBwd && nvec > 32 * 16 && nvec <= 32 * 3 * 7)
         return layout_for(H, 3);
     if (kind == kBwd && nvec <= 32 * 24)
@@ -209,6 +242,8 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int nten
     const int max_warps = (rpg == 2 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
     if (kind == kBwd && W > 1)
         groups = max_warps / W > 1 ? max_warps / W : 1;
+    else if (kind == kBwd && rl.vpt > 1)
+        groups = 4; // rows of one warp at 24 / 32 columns: three CTAs of four groups per SM
     else if (kind == kFwd && ntens == 1 && rl.vpt == 2 && W > 1)
         groups = max_warps / W > 1 ? max_warps / W : 1; // plain forward: see the cap below
     else
@@ -410,6 +445,53 @@ cake_status check_tensor(const cake_tensor *t, const cake_shape *s)
     return CAKE_OK;
 }
 
+// An output tensor: as check_tensor, and no two of its rows overlap (a
+// kernel writes every row once, so rows that share memory would race).  The
+// dimensions with more than one index, in ascending stride order, must each
+// step past everything the smaller ones span.
+cake_status check_out_tensor(const cake_tensor *t, const cake_shape *s)
+{
+    cake_status st = check_tensor(t, s);
+    if (st != CAKE_OK)
+        return st;
+    int64_t dims[2][2] = {{s->tokens, t->stride_token}, {s->heads, t->stride_head}};
+    if (dims[0][1] > dims[1][1]) {
+        std::swap(dims[0][0], dims[1][0]);
+        std::swap(dims[0][1], dims[1][1]);
+    }
+    int64_t span = s->hidden; // elements one index of the dimensions seen so far covers
+    for (auto &d : dims) {
+        if (d[0] <= 1)
+            continue;
+        if (d[1] < span)
+            return CAKE_ERR_INVALID;
+        span = (d[0] - 1) * d[1] + span;
+    }
+    return CAKE_OK;
+}
+
+// Byte range [lo, hi) a view's rows touch (strides are non-negative).
+std::pair<uintptr_t, uintptr_t> extent(const cake_tensor *t, const cake_shape *s)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(t->data);
+    const int64_t last = (s->tokens - 1) * t->stride_token + (s->heads > 1 ? (s->heads - 1) * t->stride_head : 0);
+    return {lo, lo + (uintptr_t)(2 * (last + s->hidden))};
+}
+
+bool overlap(const cake_tensor *a, const cake_tensor *b, const cake_shape *s)
+{
+    if (!a || !a->data || !b || !b->data)
+        return false;
+    const auto ea = extent(a, s), eb = extent(b, s);
+    return ea.first < eb.second && eb.first < ea.second;
+}
+
+bool same_view(const cake_tensor *a, const cake_tensor *b, const cake_shape *s)
+{
+    return a->data == b->data && (s->tokens <= 1 || a->stride_token == b->stride_token) &&
+           (s->heads <= 1 || a->stride_head == b->stride_head);
+}
+
 RowView make_view(const cake_tensor *t, const cake_shape *s)
 {
     RowView v{};
@@ -500,7 +582,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
                     const float *rstd, const void *w, cake_dtype w_dtype, const cake_tensor *dh,
                     const cake_tensor *dx, float *dw, void *workspace, size_t workspace_bytes,
                     int deterministic, int force_single, int force_accum, cake_stream_t stream,
-                    Phase phase = kWhole)
+                    Phase phase = kWhole, uint64_t wait_ns = kWaitLimitNs, int grid_extra = 0)
 {
     uint32_t rows = 0;
     const int has_dh = dh && dh->data;
@@ -523,10 +605,13 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     if ((reinterpret_cast<uintptr_t>(rstd) & 3u) != 0)
         return CAKE_ERR_UNSUPPORTED;
     if ((st = check_tensor(dy, shape)) != CAKE_OK || (st = check_tensor(x, shape)) != CAKE_OK ||
-        (st = check_tensor(dx, shape)) != CAKE_OK)
+        (st = check_out_tensor(dx, shape)) != CAKE_OK)
         return st;
     if (has_dh && (st = check_tensor(dh, shape)) != CAKE_OK)
         return st;
+    // dx is written while later rows of dy, x and dh are still being read
+    if (overlap(dx, dy, shape) || overlap(dx, x, shape) || (has_dh && overlap(dx, dh, shape)))
+        return CAKE_ERR_INVALID;
     const size_t need = ws_need(plan.single, H, plan.ctas);
     if (!workspace || workspace_bytes < need)
         return CAKE_ERR_WORKSPACE;
@@ -568,6 +653,8 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     }
     p.block_rows = 16;
     p.status = nullptr;
+    p.wait_ns = wait_ns;
+    p.grid_extra = grid_extra;
     cudaError_t e = launch_bwd_rows(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s);
     if (e != cudaSuccess || plan.single != kFormPair || phase == kMainOnly)
         return cuda_status(e);
@@ -631,6 +718,15 @@ extern "C" cake_status cake_rmsnorm_bwd_noalloc(const cake_shape *shape, const c
     cake_status st = check_shape(shape, &rows);
     if (st != CAKE_OK)
         return st;
+    // The scratch address is looked up for the current device, so the stream
+    // must belong to that device (a stream of another GPU would run the
+    // kernel against the other GPU's copy of the array).
+    int cur = -1, sdev = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess ||
+        cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+        return CAKE_ERR_CUDA;
+    if (sdev != cur)
+        return CAKE_ERR_INVALID;
     void *scratch = nullptr;
     if ((st = noalloc_scratch(&scratch)) != CAKE_OK)
         return st;
@@ -684,13 +780,26 @@ cake_status cake_rmsnorm_fwd(const cake_shape *shape, const cake_tensor *x,
         return CAKE_ERR_INVALID;
     if (!aligned16(w) || (reinterpret_cast<uintptr_t>(rstd) & 3u) != 0)
         return CAKE_ERR_UNSUPPORTED;
-    if ((st = check_tensor(x, shape)) != CAKE_OK || (st = check_tensor(y, shape)) != CAKE_OK)
+    if ((st = check_tensor(x, shape)) != CAKE_OK || (st = check_out_tensor(y, shape)) != CAKE_OK)
         return st;
     if (has_res) {
-        if ((st = check_tensor(residual, shape)) != CAKE_OK || (st = check_tensor(h_new, shape)) != CAKE_OK)
+        if ((st = check_tensor(residual, shape)) != CAKE_OK || (st = check_out_tensor(h_new, shape)) != CAKE_OK)
             return st;
     } else if (h_new && h_new->data) {
         return CAKE_ERR_INVALID;
+    }
+    // Outputs may not share memory with each other, nor partly with an input:
+    // a row is written only after it is read, so an output may be exactly an
+    // input view (in place) but not straddle other rows of one.
+    if (has_res && overlap(y, h_new, shape))
+        return CAKE_ERR_INVALID;
+    {
+        const cake_tensor *outs[2] = {y, has_res ? h_new : nullptr};
+        const cake_tensor *ins[2] = {x, has_res ? residual : nullptr};
+        for (const cake_tensor *o : outs)
+            for (const cake_tensor *i : ins)
+                if (o && i && overlap(o, i, shape) && !same_view(o, i, shape))
+                    return CAKE_ERR_INVALID;
     }
     const int H = (int)shape->hidden;
     const int ntens = has_res ? 2 : 1;
@@ -718,6 +827,7 @@ cake_status cake_rmsnorm_fwd(const cake_shape *shape, const cake_tensor *x,
     }
     p.rstd = rstd;
     p.status = nullptr;
+    p.wait_ns = kWaitLimitNs;
     return cuda_status(launch_fwd(p, plan.rl.vpt, plan.ctas, plan.smem,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -821,6 +931,19 @@ cake_status cake_rmsnorm_bwd_reduce(const cake_shape *shape, int has_dh, float *
     const float2 *parts = reinterpret_cast<const float2 *>(static_cast<uint8_t *>(workspace) + ws_part_off(H));
     ReduceParams rp{parts, plan.ctas, H, dw, reduce_slices(H, plan.ctas)};
     return cuda_status(launch_dw_reduce(rp, s));
+}
+
+cake_status cake_rmsnorm_bwd_timeout_test(const cake_shape *shape, const cake_tensor *dy,
+                                          const cake_tensor *x, const float *rstd, const void *w,
+                                          cake_dtype w_dtype, const cake_tensor *dx, float *dw,
+                                          void *workspace, size_t workspace_bytes,
+                                          uint32_t wait_limit_us, cake_stream_t stream)
+{
+    if (wait_limit_us < 1 || wait_limit_us > 1000000)
+        return CAKE_ERR_INVALID;
+    // the grid barrier waits for CTA count + 1 arrivals: it never completes
+    return run_bwd(shape, dy, x, rstd, w, w_dtype, nullptr, dx, dw, workspace, workspace_bytes, 1, kFormGrid, -1,
+                   stream, kWhole, (uint64_t)wait_limit_us * 1000u, 1);
 }
 
 cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, int has_extra,

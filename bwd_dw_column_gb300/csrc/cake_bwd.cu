@@ -82,7 +82,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         for (uint32_t r = c.r0 + lane * 32; r < c.r_end; r += 32 * 32)
             prefetch_l2(p.rstd + r);
         const RowView views[3] = {p.x, p.dy, p.dh};
-        produce<3>(s, L, c, views, L.ntens, p.status);
+        produce<3>(s, L, c, views, L.ntens, p.status, p.wait_ns);
         return;
     }
 
@@ -186,7 +186,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 #pragma unroll
         for (int i = 0; i < R2; ++i)
             rsn[i] = rs_of(it + kAhead, i);
-        abort = !mbar_wait(smem_addr(&s.full[st]), ph);
+        abort = !mbar_wait(smem_addr(&s.full[st]), ph, p.wait_ns);
         const uint8_t *stage = s.ring + st * s.stage_bytes;
         const uint32_t rbase = c.r0 + it * c.tile_rows + gid * R2;
         const int nrow = rbase < c.r_end ? (int)min((uint32_t)R2, c.r_end - rbase) : 0; // uniform in the group
@@ -271,8 +271,10 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                 const int tr = gid * R2 + i;
                 const float rs = rsr[0][i];
                 const float2 rs2 = make_float2(rs, rs);
-                // dx_j = rs*(g_j - xhat_j*c) = m_j*rs - h_j*kk, kk = rs^3 * tot / H
-                const float kk = __fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), __fmul_rn(tot[i], L.inv_h));
+                // dx_j = rs*(g_j - xhat_j*c) = m_j*rs - h_j*kk, kk = ((tot/H)*rs)*rs*rs:
+                // each product by rs brings kk back towards the scale of g, so no
+                // intermediate leaves FP32's range before the result does
+                const float kk = __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(tot[i], L.inv_h), rs), rs), rs);
                 const float2 nk2 = make_float2(-kk, -kk);
                 const uint4 *xs = reinterpret_cast<const uint4 *>(stage + tr * L.H * 2);
                 const uint4 *dys = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + tr * L.H * 2);
@@ -406,7 +408,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             // symmetric, so the result is the same on every lane and run.
             consumer_sync(L);
             if (threadIdx.x == 0)
-                s.flag[1] = grid_barrier(p.grid_cnt, p.grid_gen, gridDim.x);
+                s.flag[1] = grid_barrier(p.grid_cnt, p.grid_gen, gridDim.x + (uint32_t)p.grid_extra, p.wait_ns);
             consumer_sync(L);
             if (!s.flag[1]) {
                 if (threadIdx.x == 0)

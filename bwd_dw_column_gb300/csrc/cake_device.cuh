@@ -19,10 +19,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-// A wait that has not completed after this long is treated as a hang: the
-// kernel records CAKE_ERR_TIMEOUT in its status word and leaves its loop.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
-
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -75,8 +71,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for the phase with the given parity to complete.  Returns false if it
-// has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// has not completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -84,7 +80,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 3u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+        if ((i & 3u) == 0 && globaltimer_ns() - t0 > limit_ns)
             return false;
     }
 }
@@ -224,17 +220,18 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
 }
 
 // Grid-wide barrier of one thread per CTA (all CTAs co-resident: a
-// cooperative launch).  cnt counts arrivals; the last CTA to arrive resets
-// it and advances gen, which the others wait on.  Before it the caller's
-// CTA has synchronised, so the fence + add publishes the whole CTA's writes
-// (a release; the acquire loads / fence make the other CTAs' writes visible
-// to this CTA after its next barrier).  Returns false if gen has not moved
-// within kWaitLimitNs.
-__device__ __forceinline__ bool grid_barrier(uint32_t *cnt, uint32_t *gen, uint32_t nctas)
+// cooperative launch).  cnt counts arrivals; the CTA whose arrival makes
+// `target` resets it and advances gen, which the others wait on (target is
+// the CTA count; a larger one never completes, which is how the timeout test
+// makes this wait run out).  Before it the caller's CTA has synchronised, so
+// the fence + add publishes the whole CTA's writes (a release; the acquire
+// loads / fence make the other CTAs' writes visible to this CTA after its
+// next barrier).  Returns false if gen has not moved within limit_ns.
+__device__ __forceinline__ bool grid_barrier(uint32_t *cnt, uint32_t *gen, uint32_t target, uint64_t limit_ns)
 {
     const uint32_t g0 = ld_relaxed_gpu(gen);
     __threadfence();
-    if (atomicAdd(cnt, 1u) == nctas - 1) {
+    if (atomicAdd(cnt, 1u) == target - 1) {
         atomicExch(cnt, 0u);
         __threadfence();
         atomicAdd(gen, 1u);
@@ -245,7 +242,7 @@ __device__ __forceinline__ bool grid_barrier(uint32_t *cnt, uint32_t *gen, uint3
         if (ld_acquire_gpu(gen) != g0)
             return true;
         __nanosleep(64);
-        if ((i & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+        if ((i & 15u) == 0 && globaltimer_ns() - t0 > limit_ns)
             return false;
     }
 }

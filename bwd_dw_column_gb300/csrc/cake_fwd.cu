@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
 
     if (warp == consumer_warps) {
         const RowView views[2] = {p.x, p.res};
-        produce<2>(s, L, c, views, L.ntens, p.status);
+        produce<2>(s, L, c, views, L.ntens, p.status, p.wait_ns);
         return;
     }
 
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
     uint32_t slot = 0;
     uint32_t st = 0, ph = 0; // ring slot of tile `it` and the parity of its round
     for (uint32_t it = 0; it < c.ntiles && !abort; ++it) {
-        abort = !mbar_wait(smem_addr(&s.full[st]), ph);
+        abort = !mbar_wait(smem_addr(&s.full[st]), ph, p.wait_ns);
         const uint8_t *stage = s.ring + st * s.stage_bytes;
         const uint32_t r = c.r0 + it * c.tile_rows + gid;
         if (r < c.r_end) { // uniform across the group

@@ -7,6 +7,12 @@
 
 namespace cake {
 
+// Default limit of every bounded wait in the kernels: one that has not
+// completed after this long is treated as a hang -- the kernel records
+// CAKE_ERR_TIMEOUT in its status word and leaves its loop.  The limit travels
+// in the launch parameters (wait_ns), so a test can shorten it.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
 // Bytes at the start of a CTA's dynamic shared memory for the mbarriers, the
 // per-row reduction slots and flags; the staging ring follows.
 constexpr int kMiscBytes = 1024;
@@ -95,6 +101,7 @@ struct FwdParams {
     int hn_uniform;
     float *rstd;
     int *status;
+    uint64_t wait_ns;   // limit of every bounded wait
 };
 
 struct BwdParams {
@@ -117,6 +124,9 @@ struct BwdParams {
     unsigned int *arrivals; // single: CTA arrival counter (zero between calls)
     int block_rows;     // blocked accumulation: rows per FP32 block
     int *status;
+    uint64_t wait_ns;   // limit of every bounded wait
+    int grid_extra;     // grid form: arrivals its barrier expects beyond the CTA count (0; the
+                        // timeout test sets 1 so that the barrier never completes)
 };
 
 struct ReduceParams {

@@ -13,7 +13,7 @@
 //     butterfly plus, when W > 1, a fixed-order sum of the W warp partials
 //     through shared memory behind one named barrier per row.
 // No CTA ever waits on another CTA.  Every mbarrier wait is bounded
-// (kWaitLimitNs); a wait that runs out sets the status word to
+// (the launch's wait_ns); a wait that runs out sets the status word to
 // CAKE_ERR_TIMEOUT and the CTA leaves its loop after draining its own copies.
 #pragma once
 
@@ -84,7 +84,7 @@ __device__ __forceinline__ Chunk cta_chunk(const Layout &L)
 // views[i] is the i-th staged tensor.  Returns false on a timeout.
 template <int NT>
 __device__ __forceinline__ void produce(const Smem &s, const Layout &L, const Chunk &c,
-                                       const RowView (&views)[NT], int ntens, int *status)
+                                       const RowView (&views)[NT], int ntens, int *status, uint64_t wait_ns)
 {
     const int lane = threadIdx.x & 31;
     const uint64_t pol = policy_evict_first();
@@ -95,7 +95,7 @@ __device__ __forceinline__ void produce(const Smem &s, const Layout &L, const Ch
     for (; it < c.ntiles; ++it) {
         if (it >= (uint32_t)L.stages) {
             // the previous round of this slot was released by the consumers
-            bool got = mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u);
+            bool got = mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, wait_ns);
             got = __all_sync(0xffffffffu, got);
             if (!got) {
                 if (lane == 0)
@@ -136,7 +136,7 @@ __device__ __forceinline__ void produce(const Smem &s, const Layout &L, const Ch
     const uint32_t issued = it;
     const uint32_t first = issued > (uint32_t)L.stages ? issued - L.stages : 0;
     for (uint32_t j = first; j < issued; ++j) {
-        if (!mbar_wait(smem_addr(&s.full[j % L.stages]), (j / L.stages) & 1)) {
+        if (!mbar_wait(smem_addr(&s.full[j % L.stages]), (j / L.stages) & 1, wait_ns)) {
             if (lane == 0)
                 set_status(status, kStatusTimeout);
         }

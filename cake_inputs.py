@@ -163,6 +163,15 @@ SWEEP_T = (4096, 44032, 65536, 131072)
 SWEEP_FAMILIES = ("gauss", "outlier", "offset")
 SWEEP_SEEDS = 60
 
+# The sweep's shapes as benchmark workloads (gaussian family, seed 0): a BF16
+# weight at every point, and an FP32 weight at T = 65536.
+for _H in SWEEP_H:
+    for _T in SWEEP_T:
+        WORKLOADS.setdefault(f"h{_H}_t{_T}_sweep", dict(kind="plain", T=_T, H=_H, family="gauss",
+                                                         w_dtype=torch.bfloat16, dy_std=1.0))
+    WORKLOADS[f"h{_H}_t65536_sweep_w32"] = dict(kind="plain", T=65536, H=_H, family="gauss",
+                                                w_dtype=torch.float32, dy_std=1.0)
+
 
 def make(name: str, seed: int = 0, device="cpu", **overrides) -> dict:
     """Build one named workload (``WORKLOADS``), optionally with overridden sizes."""

@@ -43,6 +43,10 @@
  *     activation base pointer and w must be 16-byte aligned and every stride a
  *     multiple of 8 elements (16 bytes), else CAKE_ERR_UNSUPPORTED.
  *   - rows = T * nh must be below 2^31.
+ *   - Output views (y, h_new, dx) may not have rows that share memory, else
+ *     CAKE_ERR_INVALID.  dx may not share memory with dy, x or dh; y and
+ *     h_new may not share memory with each other, and share memory with an
+ *     input only as exactly the same view (in place); else CAKE_ERR_INVALID.
  *   - Return codes come from host-side validation and from the CUDA launch
  *     (cudaGetLastError).  Faults that happen later on the device surface at
  *     the caller's next synchronisation, as with any CUDA call; the kernels'
@@ -132,7 +136,8 @@ cake_status cake_rmsnorm_bwd_workspace_init(void *workspace, size_t workspace_by
  * the saved h_new on the residual route).  rstd: the forward's FP32 rstd.
  * dh: NULL, or the gradient that reaches h_new directly on the residual route
  * (added into dx, which is then the gradient of both x and residual).
- * dx: output rows (may not alias dy, x or dh).  dw: [H] FP32, overwritten.
+ * dx: output rows (may not share memory with dy, x or dh).  dw: [H] FP32,
+ * overwritten.
  * deterministic != 0: the main + fixed-order reduce pair; dw is bitwise
  * reproducible for equal inputs and shape.  deterministic == 0: the window
  * table may pick a single-kernel form where one is faster than the pair, and
@@ -207,9 +212,10 @@ typedef struct {
  * dtype, mode and residual gradient.  force_single (0 to 3 as in
  * cake_variant.single) / force_accum (-1 = let the table decide) override
  * the table, as the tests that sweep every variant do; deterministic = 1
- * refuses force_single = 1 with CAKE_ERR_INVALID; force_single = 2 needs the
- * 8-columns-per-thread layout with one row per group (H <= 6144 except
- * 3080 .. 5376), else CAKE_ERR_UNSUPPORTED.
+ * refuses force_single = 1 with CAKE_ERR_INVALID; force_single = 2 needs a
+ * row layout of 8 columns per thread with one row per group (the table's
+ * choice for H <= 512 and a few widths between 1032 and 1144), else
+ * CAKE_ERR_UNSUPPORTED.
  */
 cake_status cake_rmsnorm_bwd_select(const cake_shape *shape, cake_dtype w_dtype,
                                     int deterministic, int has_dh, int force_single,
@@ -241,7 +247,8 @@ cake_status cake_rmsnorm_bwd_forced(const cake_shape *shape, const cake_tensor *
  *     scratch is too small); other argument errors as cake_rmsnorm_bwd.
  *   - The first call on a device looks up the array's device address with
  *     that device current and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  `stream` must belong to the current device, else
+ *     CAKE_ERR_INVALID.
  *   - Every call clears the scratch it uses (an asynchronous memset) before
  *     its kernel.  All calls share the one array, so calls that overlap on
  *     the GPU (different streams, or several host threads) race: order them
@@ -253,6 +260,30 @@ cake_status cake_rmsnorm_bwd_noalloc(const cake_shape *shape, const cake_tensor 
                                      const cake_tensor *x, const float *rstd, const void *w,
                                      cake_dtype w_dtype, const cake_tensor *dh,
                                      const cake_tensor *dx, float *dw, cake_stream_t stream);
+
+/* ---- testing the timeout path ----------------------------------------------
+ * No counterpart in the pages: an addition of this library, for tests.
+ *
+ * Every wait in the kernels is bounded; one that runs out sets the device
+ * status to CAKE_ERR_TIMEOUT and the kernel returns instead of hanging.  This
+ * entry point makes such a wait run out on purpose, from the host, so that a
+ * test can check that path: it runs the cooperative grid form of the
+ * backward (cake_rmsnorm_bwd_forced with force_single = 3) with its grid
+ * barrier expecting one arrival more than the launch has CTAs, and with every
+ * bounded wait limited to wait_limit_us microseconds (1 .. 1000000, else
+ * CAKE_ERR_INVALID).  The barrier cannot complete, so each CTA gives up after
+ * the limit, sets CAKE_ERR_TIMEOUT and returns: the launch ends by itself and
+ * the CUDA context stays usable.  dx is written; dw is not.  The barrier's
+ * arrival counter is left non-zero, so re-initialise the workspace
+ * (cake_rmsnorm_bwd_workspace_init) before its next use, and read and clear
+ * the status with cake_rmsnorm_device_status(&code, 1).  Other arguments as
+ * cake_rmsnorm_bwd_forced.
+ */
+cake_status cake_rmsnorm_bwd_timeout_test(const cake_shape *shape, const cake_tensor *dy,
+                                          const cake_tensor *x, const float *rstd, const void *w,
+                                          cake_dtype w_dtype, const cake_tensor *dx, float *dw,
+                                          void *workspace, size_t workspace_bytes,
+                                          uint32_t wait_limit_us, cake_stream_t stream);
 
 /*
  * Diagnostics: for the kernel a call with these arguments would launch, the

@@ -25,3 +25,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    from tests import report
+    lines = report.summary_lines()
+    if lines:
+        terminalreporter.section("parity against the FP64 oracle (dx in BF16 steps, dw as a fraction of its budget)")
+        for line in lines:
+            terminalreporter.write_line(line)
+    path = report.write()
+    if path:
+        terminalreporter.write_line(f"parity records written to {path}")

@@ -195,21 +195,72 @@ def _bwd(cake, shape, dy, x, rstd, w, dh, dx, dw, ws, nbytes, det=1, wd=0):
 
 
 def test_bwd_validation(cake):
-    A = 0x100000
+    A, B = 0x100000, 0x10000000  # inputs at A, dx at B (1.2 MB of rows apart)
     shape = _S(300, 1, 2048)
     need = cake.cake_rmsnorm_bwd_workspace_size((300, 1, 2048))
     t = lambda: _T(A, 2048)
-    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A, 4096) == 3          # workspace too small
-    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, None, need) == 3       # no workspace
-    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A + 16, need) == 2     # workspace not 256-B aligned
-    assert _bwd(cake, shape, t(), t(), None, A, None, t(), A, A, need) == 1       # no rstd
-    assert _bwd(cake, shape, t(), t(), A, A, None, t(), None, A, need) == 1       # no dw
-    assert _bwd(cake, shape, _T(A, 2040), t(), A, A, None, t(), A, A, need) == 2  # rows overlap
-    assert _bwd(cake, _S(300, 1, 2044), t(), t(), A, A, None, t(), A, A, need) == 2
-    assert _bwd(cake, shape, t(), t(), A, A, None, t(), A, A, need, wd=3) == 1
+    o = lambda: _T(B, 2048)
+    assert _bwd(cake, shape, t(), t(), A, A, None, o(), A, A, 4096) == 3          # workspace too small
+    assert _bwd(cake, shape, t(), t(), A, A, None, o(), A, None, need) == 3       # no workspace
+    assert _bwd(cake, shape, t(), t(), A, A, None, o(), A, A + 16, need) == 2     # workspace not 256-B aligned
+    assert _bwd(cake, shape, t(), t(), None, A, None, o(), A, A, need) == 1       # no rstd
+    assert _bwd(cake, shape, t(), t(), A, A, None, o(), None, A, need) == 1       # no dw
+    assert _bwd(cake, shape, _T(A, 2040), t(), A, A, None, o(), A, A, need) == 2  # rows overlap
+    assert _bwd(cake, _S(300, 1, 2044), t(), t(), A, A, None, o(), A, A, need) == 2
+    assert _bwd(cake, shape, t(), t(), A, A, None, o(), A, A, need, wd=3) == 1
     heads = _S(16, 24, 256)
     assert _bwd(cake, heads, _T(A, 24 * 256, 256), _T(A, 24 * 512, 100), A, A, None,
-                _T(A, 24 * 256, 256), A, A, 1 << 24) == 2                           # head stride not 16 B
+                _T(B, 24 * 256, 256), A, A, 1 << 24) == 2                           # head stride not 16 B
+
+
+def test_bwd_rejects_dx_sharing_memory(cake):
+    A, B, D = 0x100000, 0x10000000, 0x20000000
+    shape = _S(300, 1, 2048)
+    rows = 300 * 2048 * 2
+    t = lambda a: _T(a, 2048)
+    # dx is dy, or x, or dh, or straddles the end of x: rejected before the workspace check
+    assert _bwd(cake, shape, t(A), t(B), A, A, None, t(A), A, A, 0) == 1
+    assert _bwd(cake, shape, t(A), t(B), A, A, None, t(B), A, A, 0) == 1
+    assert _bwd(cake, shape, t(A), t(B), A, A, t(D), t(D), A, A, 0) == 1
+    assert _bwd(cake, shape, t(A), t(B), A, A, None, t(B + rows - 4096), A, A, 0) == 1
+    # disjoint dx gets as far as the workspace check
+    assert _bwd(cake, shape, t(A), t(B), A, A, t(D), t(B + rows), A, A, 0) == 3
+
+
+def test_bwd_rejects_output_rows_that_overlap(cake):
+    A, B = 0x100000, 0x10000000
+    heads = _S(16, 24, 256)
+    x = _T(A, 24 * 256, 256)
+    assert _bwd(cake, heads, x, x, A, A, None, _T(B, 24 * 256, 256), A, A, 0) == 3   # contiguous [T, 24, 256]
+    assert _bwd(cake, heads, x, x, A, A, None, _T(B, 256, 256), A, A, 0) == 1        # token rows repeat heads
+    assert _bwd(cake, heads, x, x, A, A, None, _T(B, 0, 256), A, A, 0) == 1          # every token on one row set
+    assert _bwd(cake, heads, x, x, A, A, None, _T(B, 24 * 512, 512), A, A, 0) == 3   # strided, disjoint
+    # head-major [nh, T, 256] storage: heads step past all tokens
+    assert _bwd(cake, heads, x, x, A, A, None, _T(B, 256, 16 * 256), A, A, 0) == 3
+    assert _bwd(cake, heads, x, x, A, A, None, _T(B, 256, 8 * 256), A, A, 0) == 1
+
+
+def test_fwd_rejects_outputs_sharing_memory(cake):
+    A, B, C = 0x100000, 0x10000000, 0x20000000
+    s = _S(4, 1, 64)
+    t = lambda a: _T(a, 64)
+    # y over x exactly (in place) is allowed: it gets past validation
+    assert _fwd(cake, s, t(A), None, A, t(A), None, C) not in (1, 2)
+    assert _fwd(cake, s, t(A), None, A, t(A + 128), None, C) == 1        # y straddles rows of x
+    assert _fwd(cake, s, t(A), t(B), A, t(C), t(C), C) == 1              # y and h_new share memory
+    assert _fwd(cake, s, t(A), t(B), A, t(C), t(B + 128), C) == 1        # h_new straddles the residual
+    assert _fwd(cake, s, t(A), t(B), A, t(C), t(A), C) not in (1, 2)     # h_new over x in place
+    assert _fwd(cake, _S(4, 2, 64), _T(A, 128, 64), None, A, _T(C, 64, 64), None, C) == 1  # y rows overlap
+
+
+def test_timeout_test_entry_validates_its_limit(cake):
+    lib = cake.load_library()
+    A = 0x100000
+    for limit in (0, 1000001):
+        st = lib.cake_rmsnorm_bwd_timeout_test(ctypes.byref(_S(4, 1, 256)), ctypes.byref(_T(A, 256)),
+                                               ctypes.byref(_T(A, 256)), A, A, 0, ctypes.byref(_T(A, 256)), A, A,
+                                               1 << 20, limit, None)
+        assert st == 1
 
 
 def test_row_groups_fit_named_barriers(cake):
@@ -230,23 +281,24 @@ def test_row_groups_fit_named_barriers(cake):
 def test_row_group_override_is_capped(cake, tune):
     # the tuning override cannot push a multi-warp row past the barrier ids
     code = ("import bwd_dw_column_gb300 as c, json; "
-            "print(json.dumps([c.cake_rmsnorm_bwd_select((65536, 1, H)) for H in (512, 1024, 1536)]))")
+            "print(json.dumps([c.cake_rmsnorm_bwd_select((65536, 1, H)) for H in (512, 1536, 2048, 1040)]))")
     env = dict(os.environ, CAKE_TUNE=tune)
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT, check=True)
     for v in json.loads(out.stdout.strip().splitlines()[-1]):
         assert v["warps_per_row"] > 1
         assert v["row_groups"] <= 14
-        assert v["row_groups"] * v["warps_per_row"] + 1 <= 26
+        assert v["row_groups"] * v["warps_per_row"] + 1 <= (26 if v["vec_per_thread"] == 1 else 13)
 
 
 def test_tree_form_selection(cake):
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), deterministic=True, force_single=2)
     assert v["single"] == 2 and v["vec_per_thread"] == 1
-    v = cake.cake_rmsnorm_bwd_select((1000, 1, 2048), deterministic=False, force_single=2)
+    v = cake.cake_rmsnorm_bwd_select((1000, 1, 512), deterministic=False, force_single=2)
     assert v["single"] == 2
-    with pytest.raises(cake.CakeError) as e:
-        cake.cake_rmsnorm_bwd_select((1000, 1, 8192), deterministic=True, force_single=2)
-    assert e.value.status == 2
+    for H in (2048, 8192):  # 32 and 24 columns per thread: no tree form
+        with pytest.raises(cake.CakeError) as e:
+            cake.cake_rmsnorm_bwd_select((1000, 1, H), deterministic=True, force_single=2)
+        assert e.value.status == 2
     # the workspace the size query reports holds every form, the tree included
     n = cake.cake_rmsnorm_bwd_workspace_size((32768, 4, 256))
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), force_single=2)

@@ -93,3 +93,38 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.traffic_record("bwd_rows_kernel", "w")["summary"] == "profiles/s.md"
     assert bench.recorded_traffic("bwd_rows_kernel", "stale") is None  # counters from other sources
     assert bench.traffic_record("bwd_rows_kernel", "missing") is None
+
+
+NCU_CSV = """==PROF== Connected to process 1
+"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"
+"0","1","python","h","void cake::fwd_rows_kernel<3>(cake::FwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Gbyte","9.99"
+"1","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Mbyte","800.5"
+"1","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","Mbyte","400.25"
+"1","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","usecond","200"
+"2","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Mbyte","801.5"
+"2","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","Mbyte","400.75"
+"2","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","usecond","202"
+"""
+
+
+def test_record_traffic_takes_counters_only_for_the_sources_they_came_from(tmp_path, monkeypatch):
+    import bench
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles").mkdir()
+    csv = tmp_path / "launches.csv"
+    csv.write_text(NCU_CSV)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    ls = bench.parse_ncu_csv(str(csv), "bwd_rows_kernel")
+    assert len(ls) == 2 and ls[0]["dram__bytes_read.sum"] == pytest.approx(800.5e6)
+    args = bench.parse_args(["--record-traffic", str(csv), "--workload", "w", "--hash", "0" * 16])
+    with pytest.raises(SystemExit):  # counters of other sources are refused
+        bench.record_traffic(args)
+    assert not (tmp_path / "profiles" / "traffic.json").exists()
+    args = bench.parse_args(["--record-traffic", str(csv), "--workload", "w", "--hash", h, "--summary", "s.md",
+                             "--scale", "2"])
+    bench.record_traffic(args)
+    ent = bench.traffic_record("bwd_rows_kernel", "w")
+    assert ent["source_hash"] == h and ent["launches"] == 2
+    assert ent["dram_bytes_per_launch"] == round(2 * (800.5e6 + 400.25e6 + 801.5e6 + 400.75e6) / 2)
+    assert ent["ncu_us_per_launch"] == pytest.approx(402.0)

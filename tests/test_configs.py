@@ -22,6 +22,7 @@ import torch
 
 import cake_inputs
 import oracle
+from tests import report
 from tests import tolerances as tol
 
 pytestmark = pytest.mark.gpu
@@ -62,9 +63,10 @@ def sample_rows(R, n=48, seed=0):
 
 
 def check_dx(dx_bits_rows, dx64, dyv_rows, hv_rows, w64, rin_rows, dh_rows=None):
-    strict, bounded = tol.dx_check(dx_bits_rows, dx64, dyv_rows, hv_rows, w64, rin_rows, oracle.bf16_round,
-                                   oracle.bf16_bits_to_f64, dh=dh_rows)
-    assert bounded == 0, f"dx: {strict} strict / {bounded} bounded violations"
+    rep = tol.dx_report(dx_bits_rows, dx64, dyv_rows, hv_rows, w64, rin_rows, oracle.bf16_round,
+                        oracle.bf16_bits_to_f64, dh=dh_rows)
+    assert rep["bounded"] == 0 and rep["off_cancellation"] == 0, f"dx: {rep}"
+    return rep
 
 
 def rows_of(view: oracle.View, rows, nh, H):
@@ -77,7 +79,7 @@ def rows_of(view: oracle.View, rows, nh, H):
     return oracle.bf16_bits_to_f64(a[rows // nh, rows % nh])
 
 
-def run_workload(cake, x, dy, w, eps, residual=None, dh=None, full_dx=True, sampled=None):
+def run_workload(cake, x, dy, w, eps, residual=None, dh=None, full_dx=True, sampled=None, name=None):
     T = x.shape[0]
     nh = x.shape[1] if x.dim() == 3 else 1
     H = x.shape[-1]
@@ -115,6 +117,7 @@ def run_workload(cake, x, dy, w, eps, residual=None, dh=None, full_dx=True, samp
     dhf = rows_of(dhv, dx_rows, nh, H) if dh is not None else None
     w64 = w.double().cpu().numpy()
     dx_bits = None
+    dx_rep = None
     worst = {}
     for det in (True, False):
         dws = []
@@ -125,7 +128,7 @@ def run_workload(cake, x, dy, w, eps, residual=None, dh=None, full_dx=True, samp
             b = bits(dx).reshape(R, H)
             if dx_bits is None:
                 dx_bits = b
-                check_dx(b[dx_rows], dx64, dyf, hf, w64, rin[dx_rows], dhf)
+                dx_rep = check_dx(b[dx_rows], dx64, dyf, hf, w64, rin[dx_rows], dhf)
             else:
                 assert np.array_equal(b, dx_bits)  # dx: same bits in both modes and calls
             del dx
@@ -134,28 +137,33 @@ def run_workload(cake, x, dy, w, eps, residual=None, dh=None, full_dx=True, samp
         frac = max(float(tol.dw_budget_fraction(d, dw64).max()) for d in dws)
         assert frac <= 1.0, frac
         worst["det" if det else "nondet"] = frac
+    what = name or f"T={T} nh={nh} H={H}"
+    rows_note = "every row" if full_dx else f"{len(dx_rows)} sampled rows"
+    report.record(f"full size {what}: dx of {rows_note}, dw of every column", dx=dx_rep,
+                  dw_worst=max(worst.values()), dw_det=worst["det"], dw_nondet=worst["nondet"])
     return worst
 
 
 def test_h1536_t256(cake):
     c = cake_inputs.make("h1536_t256", seed=0, device=DEV)
-    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"])
+    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], name="h1536_t256")
 
 
 def test_h2048_t65536_outlier_w32(cake):
     c = cake_inputs.make("h2048_t65536_outlier_w32", seed=0, device=DEV)
-    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"])
+    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], name="h2048_t65536_outlier_w32")
 
 
 def test_h6144_t131072_residual(cake):
     c = cake_inputs.make("h6144_t131072_res", seed=0, device=DEV)
-    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], residual=c["residual"], dh=c["dh"], full_dx=False)
+    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], residual=c["residual"], dh=c["dh"], full_dx=False,
+                 name="h6144_t131072_res")
 
 
 @pytest.mark.parametrize("name", ["heads24_t32768_strided", "heads4_t32768"])
 def test_per_head(cake, name):
     c = cake_inputs.make(name, seed=0, device=DEV)
-    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"])
+    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], name=name)
 
 
 @pytest.mark.parametrize("name", ["h4096_t65536_sweep", "h5120_t65536_sweep"])
@@ -163,4 +171,4 @@ def test_sweep_widths(cake, name):
     # the accuracy sweep's widths at T = 65536: two rows per group (H = 4096)
     # and 24 columns per thread (H = 5120); dx of sampled rows, dw of every column
     c = cake_inputs.make(name, seed=0, device=DEV)
-    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], full_dx=False)
+    run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], full_dx=False, name=name)

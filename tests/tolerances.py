@@ -42,13 +42,13 @@ U32 = 2.0 ** -24
 
 
 def dx_allowance(dy: np.ndarray, h: np.ndarray, w: np.ndarray, rstd: np.ndarray) -> np.ndarray:
-    """FP32 evaluation bound of dx = (dy*w)*rs - h*kk, kk = rs^3 * c', for
-    every element of [R, H] rows (the kernel's order of operations).
+    """FP32 evaluation bound of dx = (dy*w)*rs - h*kk, kk = ((c'*rs)*rs)*rs,
+    for every element of [R, H] rows (the kernel's order of operations).
 
-    g = dy*w is rounded once; kk carries the roundings of rs*rs, *rs, the sum
-    c' = (1/H) sum g*h (at most 64*u*sum|g*h|/H: an FMA chain per thread, a
-    5-level butterfly, at most 24 warp partials) and the products, about 6u
-    relative in all, then h*kk and the final FMA round once more each.
+    g = dy*w is rounded once; kk carries the sum c' = (1/H) sum g*h (at most
+    64*u*sum|g*h|/H: an FMA chain per thread, a 5-level butterfly, at most 24
+    warp partials), the product by 1/H and the three products by rs, about 6u
+    relative in all; then h*kk and the final FMA round once more each.
     """
     rs = rstd.astype(np.float64)[:, None]
     g = dy * w[None, :]
@@ -60,23 +60,50 @@ def dx_allowance(dy: np.ndarray, h: np.ndarray, w: np.ndarray, rstd: np.ndarray)
     return rs * (2 * U32 * (np.abs(g) + np.abs(t)) + 8 * U32 * np.abs(xh * c) + np.abs(xh) * dc)
 
 
-def dx_check(dx_bits: np.ndarray, dx64: np.ndarray, dy: np.ndarray, h: np.ndarray, w: np.ndarray,
-             rstd: np.ndarray, bf16_round, bf16_to_f64, dh: np.ndarray | None = None):
-    """(strict, bounded) violation counts of the kernel's BF16 dx against FP64.
+# A dx element sits on cancellation when |dx64| is below 2^-8 of the scale
+# of the terms that produce it, rs*(|g| + |xhat*c|) (+ |dh|): there one BF16
+# step of dx is smaller than FP32's rounding of those terms.
+CANCELLATION = 2.0 ** -8
 
-    strict: more than one BF16 step from RNE_bf16(dx64).
-    bounded: additionally farther from dx64 than one BF16 ulp plus the FP32
-    evaluation bound of the expression (cancellation can make the exact
-    BF16 rounding of a tiny dx unreachable from FP32 arithmetic).
+
+def dx_report(dx_bits: np.ndarray, dx64: np.ndarray, dy: np.ndarray, h: np.ndarray, w: np.ndarray,
+              rstd: np.ndarray, bf16_round, bf16_to_f64, dh: np.ndarray | None = None) -> dict:
+    """Counts of the kernel's BF16 dx against FP64.
+
+    n: elements compared; max_ulp: largest distance in BF16 steps from
+    RNE_bf16(dx64); strict: elements more than one step away (the literal
+    1-ulp bar); bounded: strict elements also farther from dx64 than one BF16
+    ulp plus the FP32 evaluation bound of the expression (cancellation can
+    make the exact BF16 rounding of a tiny dx unreachable from FP32
+    arithmetic); off_cancellation: strict elements that are not on
+    cancellation (|dx64| >= 2^-8 of the terms' scale).  The parity bar is
+    bounded == 0 and off_cancellation == 0.
     """
     ref = bf16_round(dx64)
     dist = ulp_distance(dx_bits, ref)
+    out = {"n": int(dist.size), "max_ulp": int(dist.max(initial=0)), "strict": 0, "bounded": 0,
+           "off_cancellation": 0}
     strict = dist > 1
     if not strict.any():
-        return 0, 0
+        return out
     err = np.abs(bf16_to_f64(dx_bits) - dx64)
     allow = bf16_ulp(dx64) + dx_allowance(dy, h, w, rstd)
+    rs = rstd.astype(np.float64)[:, None]
+    g = dy * w[None, :]
+    xh = h * rs
+    c = (g * xh).sum(axis=1, keepdims=True) / h.shape[1]
+    scale = rs * (np.abs(g) + np.abs(xh * c))
     if dh is not None:
         allow = allow + 2 * U32 * np.abs(dx64)
+        scale = scale + np.abs(dh)
     bounded = strict & (err > allow)
-    return int(strict.sum()), int(bounded.sum())
+    off = strict & (np.abs(dx64) >= CANCELLATION * scale)
+    out.update(strict=int(strict.sum()), bounded=int(bounded.sum()), off_cancellation=int(off.sum()))
+    return out
+
+
+def dx_check(dx_bits: np.ndarray, dx64: np.ndarray, dy: np.ndarray, h: np.ndarray, w: np.ndarray,
+             rstd: np.ndarray, bf16_round, bf16_to_f64, dh: np.ndarray | None = None):
+    """(strict, bounded) violation counts of ``dx_report``."""
+    r = dx_report(dx_bits, dx64, dy, h, w, rstd, bf16_round, bf16_to_f64, dh=dh)
+    return r["strict"], r["bounded"]
