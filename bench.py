@@ -89,8 +89,11 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="time this workload only (default: the headline + configs)")
     ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --profile: the workload's shape at this many tokens (a smaller case for ncu)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["det", "nondet", "fwd", "main", "all"], default=None,
+    ap.add_argument("--profile", choices=["det", "nondet", "fwd", "main", "single_atomic", "single_grid",
+                                          "single_cluster", "all"], default=None,
                     help="run only the named loop(s) with few launches (for ncu); prints per-call times")
     ap.add_argument("--accum", choices=sorted(ACCUM), default=None,
                     help="with --profile: force the per-thread dw accumulation form")
@@ -377,11 +380,13 @@ class Workload:
     Each step callable comes with the number of library kernels it launches
     and its algorithmic bytes."""
 
-    def __init__(self, cake, torch, name, dev, seed=0, accum=None):
+    def __init__(self, cake, torch, name, dev, seed=0, accum=None, tokens=None):
         import cake_inputs
 
-        self.name, self.spec = name, cake_inputs.WORKLOADS[name]
-        case = cake_inputs.make(name, seed=seed, device=dev)
+        self.name, self.spec = name, dict(cake_inputs.WORKLOADS[name])
+        if tokens:
+            self.spec["T"] = tokens
+        case = cake_inputs.make(name, seed=seed, device=dev, **({"T": tokens} if tokens else {}))
         self.case = case
         x, dy, w, eps = case["x"], case["dy"], case["w"], case["eps"]
         res, dh = case.get("residual"), case.get("dh")
@@ -437,7 +442,9 @@ class Workload:
             if not suffix:
                 va = variant(False, ddh is not None, 1)
                 vg = variant(True, ddh is not None, 3)
+                vc = variant(True, ddh is not None, 4)
                 self.steps["single_atomic"] = (forced(1, ddh), 1, nb["single"], va)
+                self.steps["single_cluster"] = (forced(4, ddh), 1, nb["rows_only"], vc)
                 self.steps["single_grid"] = (forced(3, ddh), 1,
                                              workload_bytes(self.R, self.H, wb, vg["ctas"], dh=ddh is not None)["pair"],
                                              vg)
@@ -648,7 +655,7 @@ def run_profile(args):
     import bwd_dw_column_gb300 as cake
 
     dev = torch.device("cuda", 0)
-    wl = Workload(cake, torch, args.workload or HEADLINE, dev, accum=args.accum)
+    wl = Workload(cake, torch, args.workload or HEADLINE, dev, accum=args.accum, tokens=args.tokens)
     names = ["fwd", "det", "nondet"] if args.profile == "all" else [args.profile]
     out = {}
     stream = torch.cuda.current_stream()
@@ -664,7 +671,7 @@ def run_profile(args):
         ts = [t * 1e3 for t in time_loop(torch, fn, args.steps, args.warmup, None, stream)]
         out[n] = {"us_median": round(statistics.median(ts), 2), "us_min": round(min(ts), 2)}
     assert cake.cake_rmsnorm_device_status() == 0
-    print(json.dumps({"profile": wl.name, "accum": args.accum, "us_per_call": out,
+    print(json.dumps({"profile": wl.name, "tokens": wl.T, "accum": args.accum, "us_per_call": out,
                       "source_hash": kernel_source_hash()}), flush=True)
 
 

@@ -53,17 +53,21 @@ cudaError_t ensure_smem_attr(const void *kernel, size_t smem)
 constexpr int kSMs = 152;
 constexpr size_t kSmemPerSM = 220 * 1024; // budget for the rings of co-resident CTAs
 constexpr int kMaxStages = 16;
+// CTAs in the cluster form's one cluster (the portable maximum).
+constexpr int kClusterCTAs = 8;
 
 enum Kind { kFwd = 0, kBwd = 1 };
 
 // Developer override of the table, for tuning sweeps: CAKE_TUNE holds
-// comma-separated key=value pairs among vpt, groups, cps, stages (backward)
-// and fvpt, fgroups, fcps, fstages (forward).  Unset, the table below rules.
+// comma-separated key=value pairs among vpt, groups, cps, stages, rpg, form,
+// cluster (backward) and fvpt, fgroups, fcps, fstages (forward).  Unset, the
+// table below rules.
 // A different row layout (vpt) changes the reduction order and therefore the
 // bits of dx / y / rstd; a different cps or groups changes the pair's
 // partition and therefore the bits of the deterministic dw.
 struct Tune {
     int v[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages, rpg, form+1]
+    int cluster = 0;                                         // cluster form: CTAs per cluster
 };
 
 static Tune parse_tune(const char *t)
@@ -84,6 +88,8 @@ static Tune parse_tune(const char *t)
             for (int i = 0; i < 6; ++i)
                 if (strlen(keys[k][i]) == klen && strncmp(p, keys[k][i], klen) == 0)
                     r.v[k][i] = i == 5 ? val + 1 : val;
+        if (klen == 7 && strncmp(p, "cluster", 7) == 0 && val >= 1 && val <= kMaxCluster)
+            r.cluster = val;
         const char *comma = strchr(eq, ',');
         if (!comma)
             break;
@@ -335,6 +341,19 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     p.ctas = p.rows_per_cta ? (int)((rows + p.rows_per_cta - 1) / p.rows_per_cta) : 0;
     p.single = single;
     p.dwm = dwm;
+    if (single == kFormCluster && rows > 0) {
+        // one cluster of CTAs over all rows (at least one tile each)
+        int C = tune().cluster > 0 ? tune().cluster : kClusterCTAs;
+        const uint32_t by_tiles = (rows + tile - 1) / tile;
+        if ((uint32_t)C > by_tiles)
+            C = (int)by_tiles;
+        p.rows_per_cta = (rows + C - 1) / C;
+        p.ctas = (int)((rows + p.rows_per_cta - 1) / p.rows_per_cta);
+        // its partial lives in the drained ring
+        const size_t part = fixed + (size_t)H * 8;
+        if (part > p.smem)
+            p.smem = part;
+    }
     return p;
 }
 
@@ -395,6 +414,8 @@ static size_t ws_tree_off(int H, int ctas) { return align256(ws_size(H, ctas, 1)
 // the pair its partials, the tree its partials and the group totals.
 static size_t ws_need(int form, int H, int ctas)
 {
+    if (form == kFormCluster)
+        return 0; // the partials stay in the cluster's shared memory
     if (form == kFormAtomic)
         return kWsHeader + (size_t)H * 8;
     if (form == kFormTree)
@@ -557,7 +578,7 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
     cake_status st = check_shape(shape, rows);
     if (st != CAKE_OK)
         return st;
-    if (force_single > kFormGrid || force_accum > CAKE_DW_KAHAN)
+    if (force_single > kFormCluster || force_accum > CAKE_DW_KAHAN)
         return CAKE_ERR_INVALID;
     if (deterministic && force_single == kFormAtomic)
         return CAKE_ERR_INVALID;
@@ -613,7 +634,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     if (overlap(dx, dy, shape) || overlap(dx, x, shape) || (has_dh && overlap(dx, dh, shape)))
         return CAKE_ERR_INVALID;
     const size_t need = ws_need(plan.single, H, plan.ctas);
-    if (!workspace || workspace_bytes < need)
+    if (need > 0 && (!workspace || workspace_bytes < need))
         return CAKE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return CAKE_ERR_UNSUPPORTED;
@@ -634,13 +655,15 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.dx_uniform = dxv.uniform;
     p.dw = dw;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    p.arrivals = reinterpret_cast<unsigned int *>(ws);
-    p.acc = reinterpret_cast<double *>(ws + ws_acc_off());
-    p.partials = reinterpret_cast<float2 *>(ws + ws_part_off(H));
-    p.tree_cnt = reinterpret_cast<unsigned int *>(ws) + 1;
-    p.group_totals = reinterpret_cast<float2 *>(ws + ws_tree_off(H, plan.ctas));
-    p.grid_cnt = reinterpret_cast<unsigned int *>(ws) + kGridWords;
-    p.grid_gen = reinterpret_cast<unsigned int *>(ws) + kGridWords + 1;
+    if (ws) { // (the cluster form uses none of it)
+        p.arrivals = reinterpret_cast<unsigned int *>(ws);
+        p.acc = reinterpret_cast<double *>(ws + ws_acc_off());
+        p.partials = reinterpret_cast<float2 *>(ws + ws_part_off(H));
+        p.tree_cnt = reinterpret_cast<unsigned int *>(ws) + 1;
+        p.group_totals = reinterpret_cast<float2 *>(ws + ws_tree_off(H, plan.ctas));
+        p.grid_cnt = reinterpret_cast<unsigned int *>(ws) + kGridWords;
+        p.grid_gen = reinterpret_cast<unsigned int *>(ws) + kGridWords + 1;
+    }
     // the accumulator banks that fit the given workspace (the built-in
     // scratch of the allocation-free entry point may hold fewer than 8)
     {
@@ -655,6 +678,7 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.status = nullptr;
     p.wait_ns = wait_ns;
     p.grid_extra = grid_extra;
+    p.cluster = plan.single == kFormCluster ? plan.ctas : 0;
     cudaError_t e = launch_bwd_rows(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s);
     if (e != cudaSuccess || plan.single != kFormPair || phase == kMainOnly)
         return cuda_status(e);

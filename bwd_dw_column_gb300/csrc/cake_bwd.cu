@@ -1,42 +1,10 @@
-// cake_bwd.cu -- training RMSNorm backward for sm_103a.
-//
-// Per row (the standard RMSNorm gradient; the pages fix the outputs and their
-// dtypes -- dx BF16, dw FP32 -- in the "Speedups ... GB300 windows" commit
-// (#8577) quoted on the PR #8208 page, intro):
-//   g_j = dy_j * w_j, xhat_j = h_j * rstd, c = (1/H) sum_j g_j * xhat_j,
-//   dx_j = bf16(rstd * (g_j - xhat_j * c) [+ dh_j]),
-// and over rows, the FP32 column sum dw_j = sum_r dy_rj * h_rj * rstd_r.
-//
-// The two backward forms the pages describe, and two more one-kernel forms:
-//   * the deterministic pair (#8577 commit, intro: a main kernel, then a
-//     fixed-order dw reduce): `bwd_rows_kernel<..., FORM=0, ...>` writes one
-//     compensated (hi, lo) dw partial per CTA into the workspace, then
-//     `dw_reduce_kernel` sums the partials of each column in a fixed order
-//     (programmatic dependent launch hides its launch);
-//   * the single kernel (#8208 page, description: FP64 dw column sums, not
-//     bitwise reproducible): FORM=1 adds each CTA's partial into FP64 column
-//     accumulators with L2 atomics; the CTA that arrives last converts them to
-//     FP32 dw and zeroes the accumulators and the arrival counter for the next
-//     call.  Nobody waits for anybody;
-//   * the tree form (FORM=2): the last CTA of each group of CTAs sums its
-//     group's partials, and the last group the group totals, in fixed order;
-//   * the grid form (FORM=3): a cooperative launch whose CTAs meet at one
-//     bounded grid barrier, then each reduces a slice of the columns in fixed
-//     order.
-// dx is computed by the same code in every form, with a reduction order fixed
-// by the row layout (VPT, W) alone, so it is bitwise identical across modes,
-// variants and calls (#8208 page, description; the #8253 commit states that
-// dx does not change across the window edges).
-//
-// Per-thread dw accumulation over the CTA's rows (DWM), the pages' kernel
-// kinds restated: plain FP32 sums; blocked FP32 sums folded into a
-// compensated pair ("kb", PR #8899 page, window list); TwoSum per-thread sums
-// with the product's rounding error kept (#8208 page, description; #8253
-// commit, which names the TwoSum forms).
+// cake_bwd.cu -- training RMSNorm backward for sm_103a: launch dispatch over
+// the forms (instantiated in cake_bwd_<form>.cu from the template in
+// cake_bwd.cuh), the deterministic pair's fixed-order reduce kernel, and the
+// kernels' device status word.
 #include <mutex>
 
-#include "cake_launch.h"
-#include "cake_rows.cuh"
+#include "cake_bwd.cuh"
 
 namespace cake {
 
@@ -61,501 +29,6 @@ static cudaError_t status_ptr(int **out)
     }
     *out = addr[dev];
     return cudaSuccess;
-}
-
-template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1>
-__device__ __forceinline__ void bwd_rows(const BwdParams &p)
-{
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const Layout &L = p.L;
-    const Smem s = carve_smem(smem_raw, L);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int W = W1 ? 1 : L.warps_per_row; // W1: rows of one warp, known at compile time
-    const int consumer_warps = L.groups * W;
-    const Chunk c = cta_chunk(L);
-
-    init_ring(s, L);
-    pdl_wait();
-
-    if (warp == consumer_warps) {
-        // producer warp: warm L2 with this CTA's rstd segment, then stream rows
-        for (uint32_t r = c.r0 + lane * 32; r < c.r_end; r += 32 * 32)
-            prefetch_l2(p.rstd + r);
-        const RowView views[3] = {p.x, p.dy, p.dh};
-        produce<3>(s, L, c, views, L.ntens, p.status, p.wait_ns);
-        return;
-    }
-
-    const int gid = warp / W, wig = warp - gid * W;
-    const int gtid = wig * 32 + lane;
-    const int nvec = L.nvec;
-    const bool has_dh = L.ntens == 3;
-
-    // (with 8 columns per thread the element-wise staging measured 3-6 %
-    // faster over a whole T = 65536 step, although it costs up to 3 us more
-    // at small T)
-    stage_weight<VPT != 1>(s, L, p.w, p.w_f32);
-
-    // dw accumulators for this thread's columns (pairs of adjacent columns):
-    // the partial is hi + lo in every form.
-    float2 hi[VPT][4], lo[VPT][4], blk[VPT][4];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            hi[k][q] = make_float2(0.f, 0.f);
-            lo[k][q] = make_float2(0.f, 0.f);
-            blk[k][q] = make_float2(0.f, 0.f);
-        }
-    // Blocked sums keep the compensated pair in shared memory (this thread's
-    // own slots: planes [0, 2 VPT) the low parts, [2 VPT, 4 VPT) the high
-    // parts with 8 columns per thread), so the row loop holds only the block
-    // sums -- the registers of the plain sum.  Wider layouts keep the high
-    // parts in registers.
-    constexpr bool kHiSmem = DWM == CAKE_DWM_BLOCKED && VPT == 1;
-    const int nct = consumer_warps * 32;
-    auto plane = [&](int i) -> float4 & { return s.lo[i * nct + threadIdx.x]; };
-    auto get4 = [&](int i, float2 &a, float2 &b) {
-        const float4 v = plane(i);
-        a = make_float2(v.x, v.y);
-        b = make_float2(v.z, v.w);
-    };
-    auto put4 = [&](int i, float2 a, float2 b) { plane(i) = make_float4(a.x, a.y, b.x, b.y); };
-    // fold the block sums into the pair: (hi, lo) += blk, blk = 0
-    auto fold = [&]() {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            float2 h[4], l[4], e[4];
-            if constexpr (kHiSmem) {
-                get4(2 * VPT + 2 * k, h[0], h[1]);
-                get4(2 * VPT + 2 * k + 1, h[2], h[3]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    h[q] = hi[k][q];
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float2 sum;
-                two_sum2(h[q], blk[k][q], sum, e[q]);
-                h[q] = sum;
-                blk[k][q] = make_float2(0.f, 0.f);
-            }
-            get4(2 * k, l[0], l[1]);
-            get4(2 * k + 1, l[2], l[3]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                l[q] = add2(l[q], e[q]);
-            put4(2 * k, l[0], l[1]);
-            put4(2 * k + 1, l[2], l[3]);
-            if constexpr (kHiSmem) {
-                put4(2 * VPT + 2 * k, h[0], h[1]);
-                put4(2 * VPT + 2 * k + 1, h[2], h[3]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    hi[k][q] = h[q];
-            }
-        }
-    };
-    if (DWM == CAKE_DWM_BLOCKED)
-#pragma unroll
-        for (int k = 0; k < (kHiSmem ? 4 : 2) * VPT; ++k)
-            plane(k) = make_float4(0.f, 0.f, 0.f, 0.f);
-    int blk_rows = 0;
-
-    // A group owns R2 consecutive rows of every tile: gid*R2 + i.
-    auto rs_of = [&](uint32_t tile, int i) {
-        const uint32_t r = c.r0 + tile * c.tile_rows + gid * R2 + i;
-        return (tile < c.ntiles && r < c.r_end) ? __ldg(p.rstd + r) : 0.f;
-    };
-    // rstd of this group's rows, loaded kAhead tiles ahead (a register ring)
-    constexpr int kAhead = R2 == 1 ? 4 : 2;
-    float rsr[kAhead][R2];
-#pragma unroll
-    for (int d = 0; d < kAhead; ++d)
-#pragma unroll
-        for (int i = 0; i < R2; ++i)
-            rsr[d][i] = rs_of(d, i);
-
-    bool abort = false;
-    uint32_t slot = 0;
-    uint32_t st = 0, ph = 0; // ring slot of tile `it` and the parity of its round
-    for (uint32_t it = 0; it < c.ntiles && !abort; ++it) {
-        float rsn[R2];
-#pragma unroll
-        for (int i = 0; i < R2; ++i)
-            rsn[i] = rs_of(it + kAhead, i);
-        abort = !mbar_wait(smem_addr(&s.full[st]), ph, p.wait_ns);
-        const uint8_t *stage = s.ring + st * s.stage_bytes;
-        const uint32_t rbase = c.r0 + it * c.tile_rows + gid * R2;
-        const int nrow = rbase < c.r_end ? (int)min((uint32_t)R2, c.r_end - rbase) : 0; // uniform in the group
-        if (nrow > 0) {
-            // One pass over each staged row: m = dy*w and the row dot sum m*h
-            // (even / odd columns in the two lanes, in the order of k and q;
-            // then lane 0 + lane 1; then the group reduction), and the dw
-            // terms dy*h*rstd (dy*h is exact in FP32), rows in order.
-            // VPT == 1 keeps x and m in registers for the dx step; wider
-            // layouts re-read the staged row instead (fewer registers).
-            constexpr bool kKeep = VPT == 1 && KEEP;
-            float2 x2[R2][kKeep ? VPT : 1][4], m2[R2][kKeep ? VPT : 1][4];
-            float dot[R2];
-#pragma unroll
-            for (int i = 0; i < R2; ++i) {
-                dot[i] = 0.f;
-                if (i >= nrow)
-                    continue;
-                const int tr = gid * R2 + i;
-                const float rs = rsr[0][i];
-                const float2 rs2 = make_float2(rs, rs);
-                const float2 nrs2 = make_float2(-rs, -rs);
-                const uint4 *xs = reinterpret_cast<const uint4 *>(stage + tr * L.H * 2);
-                const uint4 *dys = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + tr * L.H * 2);
-                float2 dot2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int v = k * 32 * W + gtid;
-                    uint4 xr = make_uint4(0, 0, 0, 0), dr = make_uint4(0, 0, 0, 0);
-                    if (v < nvec) {
-                        xr = xs[v];
-                        dr = dys[v];
-                    }
-                    float2 w2[4];
-                    weight_pairs(s, L, v < nvec ? v : 0, w2);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 xv = bf2(word(xr, q));
-                        const float2 d2 = bf2(word(dr, q));
-                        const float2 mv = mul2(d2, w2[q]);
-                        if (kKeep) {
-                            x2[i][kKeep ? k : 0][q] = xv;
-                            m2[i][kKeep ? k : 0][q] = mv;
-                        }
-                        dot2 = fma2(mv, xv, dot2);
-                        const float2 a2 = mul2(d2, xv);
-                        if (DWM == CAKE_DWM_PLAIN) {
-                            hi[k][q] = fma2(a2, rs2, hi[k][q]);
-                        } else if (DWM == CAKE_DWM_BLOCKED) {
-                            blk[k][q] = fma2(a2, rs2, blk[k][q]);
-                        } else if (DWM == CAKE_DWM_TWOSUM) {
-                            // npr = -RN(a*rs); pe = a*rs - RN(a*rs) exactly (FMA);
-                            // Knuth's TwoSum of hi and RN(a*rs) written with npr:
-                            // s = hi + pr, e = (hi - (s - (s - hi))) + (pr - (s - hi));
-                            // lo collects e and pe
-                            const float2 npr = mul2(a2, nrs2);
-                            const float2 pe = fma2(a2, rs2, npr);
-                            const float2 sm = sub2(hi[k][q], npr);
-                            const float2 bp = sub2(sm, hi[k][q]);
-                            const float2 ap = sub2(sm, bp);
-                            const float2 e = sub2(sub2(hi[k][q], ap), add2(npr, bp));
-                            hi[k][q] = sm;
-                            lo[k][q] = add2(lo[k][q], add2(e, pe));
-                        } else {
-                            // Kahan: lo holds the negated running compensation
-                            const float2 y = fma2(a2, rs2, lo[k][q]);
-                            const float2 t = add2(hi[k][q], y);
-                            lo[k][q] = add2(sub2(hi[k][q], t), y);
-                            hi[k][q] = t;
-                        }
-                    }
-                }
-                dot[i] = __fadd_rn(dot2.x, dot2.y);
-            }
-            float tot[R2];
-            group_sum_n<R2, W1 ? 1 : 0>(dot, tot, s, L, gid, wig, lane, slot++, abort);
-
-#pragma unroll
-            for (int i = 0; i < R2; ++i) {
-                if (i >= nrow)
-                    continue;
-                const int tr = gid * R2 + i;
-                const float rs = rsr[0][i];
-                const float2 rs2 = make_float2(rs, rs);
-                // dx_j = rs*(g_j - xhat_j*c) = m_j*rs - h_j*kk, kk = ((tot/H)*rs)*rs*rs:
-                // each product by rs brings kk back towards the scale of g, so no
-                // intermediate leaves FP32's range before the result does
-                const float kk = __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(tot[i], L.inv_h), rs), rs), rs);
-                const float2 nk2 = make_float2(-kk, -kk);
-                const uint4 *xs = reinterpret_cast<const uint4 *>(stage + tr * L.H * 2);
-                const uint4 *dys = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + tr * L.H * 2);
-                const uint4 *dhs = reinterpret_cast<const uint4 *>(stage + 2 * s.tens_bytes + tr * L.H * 2);
-                uint16_t *dxrow =
-                    p.dx + out_off(p.dx_st, p.dx_sh, p.dx_row_stride, p.dx_uniform, rbase + i, L.nh);
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int v = k * 32 * W + gtid;
-                    if (v < nvec && !abort) {
-                        uint4 hv = make_uint4(0, 0, 0, 0);
-                        if (has_dh)
-                            hv = dhs[v];
-                        uint4 xr2 = make_uint4(0, 0, 0, 0), dr2 = make_uint4(0, 0, 0, 0);
-                        float2 w2[4];
-                        if (!kKeep) {
-                            xr2 = xs[v];
-                            dr2 = dys[v];
-                            weight_pairs(s, L, v, w2);
-                        }
-                        uint32_t o[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 xv = kKeep ? x2[i][kKeep ? k : 0][q] : bf2(word(xr2, q));
-                            const float2 mv = kKeep ? m2[i][kKeep ? k : 0][q] : mul2(bf2(word(dr2, q)), w2[q]);
-                            float2 d = fma2(mv, rs2, mul2(xv, nk2));
-                            if (has_dh)
-                                d = add2(d, bf2(word(hv, q)));
-                            o[q] = pack2(d);
-                        }
-                        __stcs(reinterpret_cast<uint4 *>(dxrow) + v, make_uint4(o[0], o[1], o[2], o[3]));
-                    }
-                }
-            }
-            if (DWM == CAKE_DWM_BLOCKED && (blk_rows += nrow) >= p.block_rows) {
-                blk_rows = 0;
-                fold();
-            }
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_addr(&s.empty[st]));
-        if (++st == (uint32_t)L.stages) {
-            st = 0;
-            ph ^= 1u;
-        }
-#pragma unroll
-        for (int d = 0; d + 1 < kAhead; ++d)
-#pragma unroll
-            for (int i = 0; i < R2; ++i)
-                rsr[d][i] = rsr[d + 1][i];
-#pragma unroll
-        for (int i = 0; i < R2; ++i)
-            rsr[kAhead - 1][i] = rsn[i];
-    }
-    if (abort && lane == 0)
-        set_status(p.status, kStatusTimeout);
-    if (DWM == CAKE_DWM_BLOCKED) {
-        fold();
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            get4(2 * k, lo[k][0], lo[k][1]);
-            get4(2 * k + 1, lo[k][2], lo[k][3]);
-            if constexpr (kHiSmem) {
-                get4(2 * VPT + 2 * k, hi[k][0], hi[k][1]);
-                get4(2 * VPT + 2 * k + 1, hi[k][2], hi[k][3]);
-            }
-        }
-    }
-    if (FORM == kFormPair)
-        pdl_launch_dependents();
-
-    // ---- combine the row groups' partials in group order (shared memory,
-    // [group - 1][q][vector] float4 (hi.x, lo.x, hi.y, lo.y): a warp's lanes
-    // touch consecutive 16-byte slots, free of bank conflicts)
-    consumer_sync(L);
-    float4 *comb = reinterpret_cast<float4 *>(s.ring);
-    const int ncol = nvec * 8;
-    if (L.groups > 1) {
-        if (gid > 0) {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                if (v < nvec)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        comb[((gid - 1) * 4 + q) * nvec + v] =
-                            make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
-            }
-        }
-        consumer_sync(L);
-        if (gid == 0) {
-            for (int g = 1; g < L.groups; ++g) {
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int v = k * 32 * W + gtid;
-                    if (v < nvec)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 a = comb[((g - 1) * 4 + q) * nvec + v];
-                            comp_add(hi[k][q].x, lo[k][q].x, a.x);
-                            lo[k][q].x = __fadd_rn(lo[k][q].x, a.y);
-                            comp_add(hi[k][q].y, lo[k][q].y, a.z);
-                            lo[k][q].y = __fadd_rn(lo[k][q].y, a.w);
-                        }
-                }
-            }
-        }
-    }
-
-    if (FORM != kFormAtomic) {
-        if (gid == 0) {
-            float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                if (v < nvec)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[v * 4 + q] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
-            }
-        }
-        if (FORM == kFormPair)
-            return;
-        if (FORM == kFormGrid) {
-            // ---- cooperative form: every CTA's partial is written; after
-            // the grid barrier CTA b reduces columns [b*C, (b+1)*C), one
-            // column per warp at a time: lane l sums the partials of CTAs
-            // [l*per, (l+1)*per) in ascending order (compensated), then the
-            // 32 lane sums merge in a butterfly whose every step is
-            // symmetric, so the result is the same on every lane and run.
-            consumer_sync(L);
-            if (threadIdx.x == 0)
-                s.flag[1] = grid_barrier(p.grid_cnt, p.grid_gen, gridDim.x + (uint32_t)p.grid_extra, p.wait_ns);
-            consumer_sync(L);
-            if (!s.flag[1]) {
-                if (threadIdx.x == 0)
-                    set_status(p.status, kStatusTimeout);
-                return;
-            }
-            const int P = (int)gridDim.x;
-            const int C = (ncol + P - 1) / P;
-            const int c0 = (int)blockIdx.x * C, c1 = min(ncol, c0 + C);
-            const int per = (P + 31) / 32;
-            const int q0 = lane * per, q1 = min(P, q0 + per);
-            for (int j = c0 + warp; j < c1; j += consumer_warps) {
-                float h = 0.f, l = 0.f;
-                for (int q = q0; q < q1; q += 4) {
-                    float2 v[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        v[u] = q + u < q1 ? __ldcg(p.partials + (size_t)(q + u) * ncol + j) : make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        comp_add(h, l, v[u].x);
-                        l = __fadd_rn(l, v[u].y);
-                    }
-                }
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1)
-                    comp_merge(h, l, __shfl_xor_sync(0xffffffffu, h, o), __shfl_xor_sync(0xffffffffu, l, o));
-                if (lane == 0)
-                    p.dw[j] = __fadd_rn(h, l);
-            }
-            return;
-        }
-        // ---- one-kernel fixed-order reduce: the last CTA to arrive among
-        // the kTreeGroup CTAs of its group sums their partials in CTA order
-        // into the group's total; the last group to finish sums the group
-        // totals in group order.  Nobody waits; the arithmetic order does not
-        // depend on who arrives last.
-        __threadfence();
-        consumer_sync(L);
-        const int grp = blockIdx.x / kTreeGroup;
-        const int ngroups = (gridDim.x + kTreeGroup - 1) / kTreeGroup;
-        if (threadIdx.x == 0) {
-            const int n_g = min(kTreeGroup, (int)gridDim.x - grp * kTreeGroup);
-            const unsigned prev = atomicAdd(p.tree_cnt + 1 + grp, 1u);
-            s.flag[1] = (prev == (unsigned)n_g - 1);
-        }
-        consumer_sync(L);
-        if (!s.flag[1])
-            return;
-        __threadfence();
-        const int nthr = consumer_warps * 32;
-        const int p0 = grp * kTreeGroup, p1 = min((int)gridDim.x, p0 + kTreeGroup);
-        for (int j = threadIdx.x; j < ncol; j += nthr) {
-            float2 v[kTreeGroup];
-#pragma unroll
-            for (int u = 0; u < kTreeGroup; ++u)
-                v[u] = p0 + u < p1 ? __ldcg(p.partials + (size_t)(p0 + u) * ncol + j) : make_float2(0.f, 0.f);
-            float h = 0.f, l = 0.f;
-#pragma unroll
-            for (int u = 0; u < kTreeGroup; ++u) {
-                comp_add(h, l, v[u].x);
-                l = __fadd_rn(l, v[u].y);
-            }
-            p.group_totals[(size_t)grp * ncol + j] = make_float2(h, l);
-        }
-        __threadfence();
-        consumer_sync(L);
-        if (threadIdx.x == 0) {
-            atomicExch(p.tree_cnt + 1 + grp, 0u);
-            const unsigned prev = atomicAdd(p.tree_cnt, 1u);
-            s.flag[2] = (prev == (unsigned)ngroups - 1);
-        }
-        consumer_sync(L);
-        if (!s.flag[2])
-            return;
-        __threadfence();
-        for (int j = threadIdx.x; j < ncol; j += nthr) {
-            float h = 0.f, l = 0.f;
-            for (int g2 = 0; g2 < ngroups; ++g2) {
-                const float2 v = __ldcg(p.group_totals + (size_t)g2 * ncol + j);
-                comp_add(h, l, v.x);
-                l = __fadd_rn(l, v.y);
-            }
-            p.dw[j] = __fadd_rn(h, l);
-        }
-        if (threadIdx.x == 0)
-            atomicExch(p.tree_cnt, 0u);
-        return;
-    }
-
-    // ---- single kernel: FP64 column accumulation into one of `banks` copies
-    // of the accumulators (CTA b adds into bank b % banks, which spreads the
-    // L2 atomics); the last CTA to arrive sums the banks and finalises
-    if (gid == 0) {
-        double *acc = p.acc + (size_t)(blockIdx.x % p.banks) * ncol;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * 32 * W + gtid;
-            if (v < nvec)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    atomicAdd(acc + v * 8 + 2 * q, (double)hi[k][q].x + (double)lo[k][q].x);
-                    atomicAdd(acc + v * 8 + 2 * q + 1, (double)hi[k][q].y + (double)lo[k][q].y);
-                }
-        }
-        __threadfence();
-    }
-    consumer_sync(L);
-    if (threadIdx.x == 0) {
-        const unsigned prev = atomicAdd(p.arrivals, 1u);
-        s.flag[1] = (prev == gridDim.x - 1);
-    }
-    consumer_sync(L);
-    if (s.flag[1]) {
-        __threadfence();
-        const int nthr = consumer_warps * 32;
-        for (int j = threadIdx.x; j < ncol; j += nthr) {
-            // every bank's load issued before the sum (banks in ascending order)
-            double v[kMaxAccBanks];
-#pragma unroll
-            for (int b = 0; b < kMaxAccBanks; ++b)
-                v[b] = b < p.banks ? __ldcg(p.acc + (size_t)b * ncol + j) : 0.0;
-            double sum = 0.0;
-#pragma unroll
-            for (int b = 0; b < kMaxAccBanks; ++b)
-                if (b < p.banks) {
-                    sum += v[b];
-                    p.acc[(size_t)b * ncol + j] = 0.0;
-                }
-            p.dw[j] = (float)sum;
-        }
-        if (threadIdx.x == 0)
-            atomicExch(p.arrivals, 0u);
-    }
-}
-
-// The row kernels, by row build RB: 0 one row per group; 1 two rows per
-// group (one group of up to 16 warps and the producer per CTA), keeping x and
-// dy*w of both rows in registers; 4 one row per group for rows of one warp
-// (H <= 256), with that width known to the compiler.  The bounds cap the
-// registers a thread may use so that the largest CTA fits: 72 (26 warps),
-// 96 (17 warps), 128 (13 warps).
-template <int VPT, int DWM, int FORM, int RB>
-__global__ void __launch_bounds__(RB == 1 ? kMaxThreadsR2 : kMaxThreadsFor(VPT), 1)
-    bwd_rows_kernel(const __grid_constant__ BwdParams p)
-{
-    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4>(p);
 }
 
 // Fixed-order reduction of the pair's CTA partials.  A CTA owns C columns
@@ -616,50 +89,13 @@ __global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __gr
 
 // ------------------------------------------------------------------ launch
 
-template <int VPT, int DWM, int FORM, int RB>
-static cudaError_t launch_rows(const BwdParams &p, int ctas, size_t smem, cudaStream_t stream)
+// Row build of a plan: 1 two rows per group, 4 rows of one warp at 8
+// columns per thread, 0 otherwise.
+static int row_build(const Layout &L, int vpt)
 {
-    const int threads = 32 * (p.L.groups * p.L.warps_per_row + 1);
-    auto kern = bwd_rows_kernel<VPT, DWM, FORM, RB>;
-    cudaError_t e = ensure_smem_attr((const void *)kern, smem);
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    // the grid form's CTAs wait for one another: the launch must guarantee
-    // that they are all resident at once (it fails otherwise)
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = FORM == kFormGrid ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, p);
-    if (e != cudaSuccess)
-        return e;
-    return cudaGetLastError();
-}
-
-template <int VPT, int FORM, int RB>
-static cudaError_t launch_form(const BwdParams &p, int dwm, int ctas, size_t smem, cudaStream_t stream)
-{
-    if (dwm == 0) return launch_rows<VPT, 0, FORM, RB>(p, ctas, smem, stream);
-    if (dwm == 1) return launch_rows<VPT, 1, FORM, RB>(p, ctas, smem, stream);
-    if (dwm == 2) return launch_rows<VPT, 2, FORM, RB>(p, ctas, smem, stream);
-    return launch_rows<VPT, 3, FORM, RB>(p, ctas, smem, stream);
-}
-
-template <int VPT, int RB>
-static cudaError_t launch_vpt(const BwdParams &p, int form, int dwm, int ctas, size_t smem,
-                              cudaStream_t stream)
-{
-    if (form == kFormAtomic)
-        return launch_form<VPT, kFormAtomic, RB>(p, dwm, ctas, smem, stream);
-    if (form == kFormGrid)
-        return launch_form<VPT, kFormGrid, RB>(p, dwm, ctas, smem, stream);
-    return launch_form<VPT, kFormPair, RB>(p, dwm, ctas, smem, stream);
+    if (L.rows_per_group == 2)
+        return 1;
+    return vpt == 1 && L.warps_per_row == 1 ? 4 : 0;
 }
 
 cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
@@ -671,23 +107,15 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
         if (e != cudaSuccess)
             return e;
     }
-    if (single == kFormTree)
-        return vpt == 1 && q.L.rows_per_group == 1 ? launch_form<1, kFormTree, 0>(q, dwm, ctas, smem, stream)
-                                                   : cudaErrorInvalidValue;
-    if (q.L.rows_per_group == 2) {
-        if (vpt != 1)
-            return cudaErrorInvalidValue;
-        if (32 * (q.L.groups * q.L.warps_per_row + 1) > kMaxThreadsR2)
-            return cudaErrorInvalidValue;
-        return launch_vpt<1, 1>(q, single, dwm, ctas, smem, stream);
-    }
-    if (vpt == 1 && q.L.warps_per_row == 1)
-        return launch_vpt<1, 4>(q, single, dwm, ctas, smem, stream);
-    switch (vpt) {
-    case 1: return launch_vpt<1, 0>(q, single, dwm, ctas, smem, stream);
-    case 2: return launch_vpt<2, 0>(q, single, dwm, ctas, smem, stream);
-    case 3: return launch_vpt<3, 0>(q, single, dwm, ctas, smem, stream);
-    case 4: return launch_vpt<4, 0>(q, single, dwm, ctas, smem, stream);
+    const int rb = row_build(q.L, vpt);
+    if (rb == 1 && (vpt != 1 || 32 * (q.L.groups * q.L.warps_per_row + 1) > kMaxThreadsR2))
+        return cudaErrorInvalidValue;
+    switch (single) {
+    case kFormPair: return launch_bwd_form<kFormPair>(q, vpt, rb, dwm, ctas, smem, stream);
+    case kFormAtomic: return launch_bwd_form<kFormAtomic>(q, vpt, rb, dwm, ctas, smem, stream);
+    case kFormTree: return launch_bwd_form<kFormTree>(q, vpt, rb, dwm, ctas, smem, stream);
+    case kFormGrid: return launch_bwd_form<kFormGrid>(q, vpt, rb, dwm, ctas, smem, stream);
+    case kFormCluster: return launch_bwd_form<kFormCluster>(q, vpt, rb, dwm, ctas, smem, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -712,53 +140,17 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int VPT, int DWM, int FORM, int RB>
-static cudaError_t occ_rows(int threads, size_t smem, int *n)
-{
-    const void *kern = (const void *)bwd_rows_kernel<VPT, DWM, FORM, RB>;
-    cudaError_t e = ensure_smem_attr(kern, smem);
-    if (e != cudaSuccess)
-        return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
-}
-
-template <int VPT, int FORM, int RB>
-static cudaError_t occ_form(int dwm, int threads, size_t smem, int *n)
-{
-    if (dwm == 0) return occ_rows<VPT, 0, FORM, RB>(threads, smem, n);
-    if (dwm == 1) return occ_rows<VPT, 1, FORM, RB>(threads, smem, n);
-    if (dwm == 2) return occ_rows<VPT, 2, FORM, RB>(threads, smem, n);
-    return occ_rows<VPT, 3, FORM, RB>(threads, smem, n);
-}
-
-template <int VPT, int RB>
-static cudaError_t occ_vpt(int single, int dwm, int threads, size_t smem, int *n)
-{
-    if (single == kFormAtomic)
-        return occ_form<VPT, kFormAtomic, RB>(dwm, threads, smem, n);
-    if (single == kFormGrid)
-        return occ_form<VPT, kFormGrid, RB>(dwm, threads, smem, n);
-    return occ_form<VPT, kFormPair, RB>(dwm, threads, smem, n);
-}
-
 cudaError_t occupancy_bwd(int vpt, int w, int rpg, int single, int dwm, int threads, size_t smem, int *n)
 {
-    if (single == kFormTree)
-        return vpt == 1 && rpg == 1 ? occ_form<1, kFormTree, 0>(dwm, threads, smem, n) : cudaErrorInvalidValue;
-    if (rpg == 2) {
-        if (vpt != 1)
-            return cudaErrorInvalidValue;
-        if (threads > kMaxThreadsR2)
-            return cudaErrorInvalidValue;
-        return occ_vpt<1, 1>(single, dwm, threads, smem, n);
-    }
-    if (vpt == 1 && w == 1)
-        return occ_vpt<1, 4>(single, dwm, threads, smem, n);
-    switch (vpt) {
-    case 1: return occ_vpt<1, 0>(single, dwm, threads, smem, n);
-    case 2: return occ_vpt<2, 0>(single, dwm, threads, smem, n);
-    case 3: return occ_vpt<3, 0>(single, dwm, threads, smem, n);
-    case 4: return occ_vpt<4, 0>(single, dwm, threads, smem, n);
+    const int rb = rpg == 2 ? 1 : (vpt == 1 && w == 1 ? 4 : 0);
+    if (rb == 1 && (vpt != 1 || threads > kMaxThreadsR2))
+        return cudaErrorInvalidValue;
+    switch (single) {
+    case kFormPair: return occ_bwd_form<kFormPair>(vpt, rb, dwm, threads, smem, n);
+    case kFormAtomic: return occ_bwd_form<kFormAtomic>(vpt, rb, dwm, threads, smem, n);
+    case kFormTree: return occ_bwd_form<kFormTree>(vpt, rb, dwm, threads, smem, n);
+    case kFormGrid: return occ_bwd_form<kFormGrid>(vpt, rb, dwm, threads, smem, n);
+    case kFormCluster: return occ_bwd_form<kFormCluster>(vpt, rb, dwm, threads, smem, n);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -42,11 +42,17 @@ constexpr int kConsumerBarrier = kMaxRowGroupBarriers + 1;
 // last-arriving CTAs (groups of kTreeGroup CTAs), or one cooperative kernel
 // whose CTAs meet at a grid barrier and then each reduce a slice of the
 // columns in fixed order.
+// And (kFormCluster) one cluster of up to kMaxCluster CTAs whose partials
+// stay in their own shared memory: after the cluster's CTAs have all written
+// theirs, CTA c sums slice c of the columns over every CTA's partial in CTA
+// order (distributed shared memory), with no workspace and no second kernel.
 constexpr int kFormPair = 0;
 constexpr int kFormAtomic = 1;
 constexpr int kFormTree = 2;
 constexpr int kFormGrid = 3;
+constexpr int kFormCluster = 4;
 constexpr int kTreeGroup = 16;
+constexpr int kMaxCluster = 16;
 // Copies (banks) of the single kernel's FP64 column accumulators, at most.
 constexpr int kMaxAccBanks = 8;
 
@@ -127,6 +133,7 @@ struct BwdParams {
     uint64_t wait_ns;   // limit of every bounded wait
     int grid_extra;     // grid form: arrivals its barrier expects beyond the CTA count (0; the
                         // timeout test sets 1 so that the barrier never completes)
+    int cluster;        // cluster form: CTAs in the (one) cluster, which is the whole grid
 };
 
 struct ReduceParams {

@@ -24,13 +24,36 @@ Only x/h_new, rstd and w are saved for the backward.  The forward is bitwise
 reproducible, so a checkpointed step (forward, forward recompute, backward:
 the "2xfwd+bwd" operation of the pages' GB300 tables) gives the same
 gradients as the plain step.
+
+Workspace: a backward without a caller-owned workspace takes one from a
+per-(device, stream) cache that grows to the largest size asked for, so a
+training step allocates and zero-fills it once, not on every backward.  The
+forms that need it zero leave it zero after every call, and calls on one
+stream are ordered, so reusing it is safe.
 """
 from __future__ import annotations
+
+import threading
 
 import torch
 
 from . import (cake_rmsnorm_bwd, cake_rmsnorm_bwd_workspace, cake_rmsnorm_bwd_workspace_size,
                cake_rmsnorm_fwd)
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def _cached_workspace(x: torch.Tensor, w_dtype, deterministic: bool) -> torch.Tensor:
+    """The (device, current stream) workspace, grown to fit this call."""
+    need = max(cake_rmsnorm_bwd_workspace_size(x, w_dtype, deterministic), 256)
+    key = (x.device.index, torch.cuda.current_stream(x.device).cuda_stream)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(need, dtype=torch.uint8, device=x.device)
+            _ws_cache[key] = ws
+        return ws
 
 __all__ = [
     "CakeRMSNormFunction", "cake_rmsnorm", "cake_rmsnorm_train_forward", "cake_rmsnorm_train_backward",
@@ -70,8 +93,8 @@ class CakeRMSNormFunction(torch.autograd.Function):
     ``apply(x, w, eps, residual, deterministic, workspace)``: residual and
     workspace may be None.  A caller-owned workspace (from
     ``cake_rmsnorm_train_backward_workspace``, sized for x, w's dtype and the
-    mode) saves one allocation per backward; calls sharing one workspace must
-    be stream-ordered.
+    mode) replaces the per-(device, stream) cached one; calls sharing one
+    workspace must be stream-ordered.
     """
 
     @staticmethod
@@ -95,8 +118,8 @@ class CakeRMSNormFunction(torch.autograd.Function):
         dy = dy.to(torch.bfloat16).contiguous()
         if dh is not None:
             dh = dh.to(torch.bfloat16).contiguous()
-        dx, dw = cake_rmsnorm_bwd(dy, h, rstd, w, dh if ctx.has_res else None, ctx.deterministic,
-                                  workspace=ctx.workspace)
+        ws = ctx.workspace if ctx.workspace is not None else _cached_workspace(h, w.dtype, ctx.deterministic)
+        dx, dw = cake_rmsnorm_bwd(dy, h, rstd, w, dh if ctx.has_res else None, ctx.deterministic, workspace=ws)
         gw = dw if w.dtype == torch.float32 else dw.to(w.dtype)
         return dx, gw, None, (dx if ctx.has_res else None), None, None
 

@@ -195,7 +195,11 @@ typedef struct {
                           by the last-arriving CTAs (deterministic); 3:
                           single cooperative kernel, a grid barrier, then a
                           fixed-order reduce of a column slice by every CTA
-                          (deterministic) */
+                          (deterministic); 4: single kernel of one thread-block
+                          cluster (ctas <= 16) whose CTAs keep their partials
+                          in shared memory and reduce a column slice each
+                          over the cluster's distributed shared memory, in
+                          CTA order (deterministic; no workspace) */
     int dw_accum;      /* cake_dw_accum */
     int vec_per_thread; /* 16-byte vectors of a row held by each thread */
     int warps_per_row; /* warps that share one row */
@@ -209,7 +213,7 @@ typedef struct {
 
 /*
  * Fill *out with the variant the window table picks for this shape, weight
- * dtype, mode and residual gradient.  force_single (0 to 3 as in
+ * dtype, mode and residual gradient.  force_single (0 to 4 as in
  * cake_variant.single) / force_accum (-1 = let the table decide) override
  * the table, as the tests that sweep every variant do; deterministic = 1
  * refuses force_single = 1 with CAKE_ERR_INVALID; force_single = 2 needs a

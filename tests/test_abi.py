@@ -152,7 +152,21 @@ def test_workspace_size(cake):
 
 # ------------------------------------------------------ argument validation
 # Fake, never-dereferenced device addresses: validation rejects the call
-# before any CUDA runtime call is made.
+# before any CUDA runtime call is made.  A call that passes validation would
+# launch a kernel on those addresses, so such calls are made only where no
+# GPU is present (the launch then fails with CAKE_ERR_CUDA, 4).
+
+
+def _no_gpu() -> bool:
+    import torch
+    return not torch.cuda.is_available()
+
+
+def _past_validation(call) -> None:
+    """Check that a call with fake addresses passes validation -- only where
+    there is no GPU to launch on."""
+    if _no_gpu():
+        assert call() == 4
 
 def _T(addr, st, sh=0):
     from bwd_dw_column_gb300 import _Tensor
@@ -174,7 +188,7 @@ def test_fwd_validation(cake):
     A = 0x100000
     ok_shape = _S(4, 1, 64)
     good = lambda: _T(A, 64)
-    assert _fwd(cake, ok_shape, good(), None, A, good(), None, A + 4096) != 1  # would launch (no GPU here)
+    _past_validation(lambda: _fwd(cake, ok_shape, good(), None, A, good(), None, A + 4096))
     assert _fwd(cake, None, good(), None, A, good(), None, A) == 1
     assert _fwd(cake, ok_shape, None, None, A, good(), None, A) == 1
     assert _fwd(cake, ok_shape, _T(A + 2, 64), None, A, good(), None, A) == 2      # misaligned x
@@ -245,11 +259,11 @@ def test_fwd_rejects_outputs_sharing_memory(cake):
     s = _S(4, 1, 64)
     t = lambda a: _T(a, 64)
     # y over x exactly (in place) is allowed: it gets past validation
-    assert _fwd(cake, s, t(A), None, A, t(A), None, C) not in (1, 2)
+    _past_validation(lambda: _fwd(cake, s, t(A), None, A, t(A), None, C))
     assert _fwd(cake, s, t(A), None, A, t(A + 128), None, C) == 1        # y straddles rows of x
     assert _fwd(cake, s, t(A), t(B), A, t(C), t(C), C) == 1              # y and h_new share memory
     assert _fwd(cake, s, t(A), t(B), A, t(C), t(B + 128), C) == 1        # h_new straddles the residual
-    assert _fwd(cake, s, t(A), t(B), A, t(C), t(A), C) not in (1, 2)     # h_new over x in place
+    _past_validation(lambda: _fwd(cake, s, t(A), t(B), A, t(C), t(A), C))  # h_new over x in place
     assert _fwd(cake, _S(4, 2, 64), _T(A, 128, 64), None, A, _T(C, 64, 64), None, C) == 1  # y rows overlap
 
 
@@ -288,6 +302,27 @@ def test_row_group_override_is_capped(cake, tune):
         assert v["warps_per_row"] > 1
         assert v["row_groups"] <= 14
         assert v["row_groups"] * v["warps_per_row"] + 1 <= (26 if v["vec_per_thread"] == 1 else 13)
+
+
+@pytest.mark.parametrize("T,H", [(1, 1536), (16, 1536), (256, 1536), (256, 4096), (1000, 6144), (4096, 256),
+                                 (70000, 2048)])
+def test_cluster_form_selection(cake, T, H):
+    # one cluster of at most 8 CTAs (the portable cluster size) covering every
+    # row, with room for its partial in shared memory; no workspace needed
+    v = cake.cake_rmsnorm_bwd_select((T, 1, H), deterministic=True, force_single=4)
+    assert v["single"] == 4 and 1 <= v["ctas"] <= 8
+    assert v["ctas"] * v["rows_per_cta"] >= T > (v["ctas"] - 1) * v["rows_per_cta"]
+    assert v["smem_bytes"] <= 227 * 1024 and v["smem_bytes"] >= 1024 + 4 * H + 8 * H
+    A, B = 0x100000, 0x40000000
+    # past validation with no workspace
+    _past_validation(lambda: _bwd_forced(cake, _S(T, 1, H), _T(A, H), _T(A, H), A, A, None, _T(B, H), A, None, 0, 1, 4))
+
+
+def _bwd_forced(cake, shape, dy, x, rstd, w, dh, dx, dw, ws, nbytes, det, single, accum=-1):
+    lib = cake.load_library()
+    r = lambda t: ctypes.byref(t) if t is not None else None
+    return lib.cake_rmsnorm_bwd_forced(r(shape), r(dy), r(x), rstd, w, 0, r(dh), r(dx), dw, ws, nbytes, det, single,
+                                       accum, None)
 
 
 def test_tree_form_selection(cake):

@@ -173,7 +173,7 @@ def test_fwd_empty(cake):
 
 # --------------------------------------------------------------------- bwd
 
-VARIANTS = [(f, acc) for f in (0, 1, 2, 3) for acc in (0, 1, 2, 3)]
+VARIANTS = [(f, acc) for f in (0, 1, 2, 3, 4) for acc in (0, 1, 2, 3)]
 
 
 def oracle_bwd_inputs(x, w, eps, residual=None):
@@ -373,3 +373,35 @@ def test_table_plans_only_resident_ctas(cake, H):
                         continue
                     planned, resident = cake.cake_rmsnorm_plan_occupancy((65536, 1, H), backward, extra, det, accum)
                     assert 1 <= planned <= resident, (H, backward, extra, det, accum, planned, resident)
+
+
+def test_cluster_form_needs_no_workspace(cake):
+    # the cluster form keeps its partials in the cluster's shared memory: it
+    # runs through the C ABI with no workspace at all, deterministic, and
+    # within the budget
+    from bwd_dw_column_gb300 import _Shape, _Tensor
+    import ctypes
+    T, H = 200, 2048
+    c = cake_inputs.plain_case(T, H, w_dtype=torch.float32, seed=13)
+    rin, _ = oracle_bwd_inputs(c["x"], c["w"], c["eps"])
+    xv, dyv = view_of(c["x"]), view_of(c["dy"])
+    dw64 = oracle.dw_cols(T, 1, H, dyv, xv, rin)
+    x, dy, w, r = c["x"].to(DEV), c["dy"].to(DEV), c["w"].to(DEV), torch.from_numpy(rin).to(DEV)
+    lib = cake.load_library()
+    outs = []
+    for _ in range(2):
+        dx = torch.empty_like(x)
+        dw = torch.empty(H, device=DEV)
+        st = lib.cake_rmsnorm_bwd_forced(ctypes.byref(_Shape(T, 1, H)), ctypes.byref(_Tensor(dy.data_ptr(), H, 0)),
+                                         ctypes.byref(_Tensor(x.data_ptr(), H, 0)), r.data_ptr(), w.data_ptr(), 1,
+                                         None, ctypes.byref(_Tensor(dx.data_ptr(), H, 0)), dw.data_ptr(), None, 0,
+                                         1, 4, -1, torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        torch.cuda.synchronize()
+        outs.append((dx, dw))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert float(tol.dw_budget_fraction(outs[0][1].cpu().numpy(), dw64).max()) <= 1.0
+    ref_dx, _ = cake.cake_rmsnorm_bwd(dy, x, r, w, deterministic=True)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], ref_dx)
+    assert cake.cake_rmsnorm_device_status() == 0

@@ -1,17 +1,25 @@
 """The training facade (autograd function and the pages' Python names).
 
-GPU tests check that autograd reaches exactly the results of the C ABI entry
-points, which the parity tests pin to the oracle: dx and dw bitwise, on the
-plain, residual and per-head routes, in both modes; and that a checkpointed
-step (forward, forward recompute, backward) gives the same gradient bits as
-the plain step.  The CPU tests check the names and that CPU tensors are
-rejected (there is no CPU path).
+GPU tests hold one autograd run per route to the FP64 oracle -- plain rows
+with an FP32 and a BF16 weight, the residual route with a gradient into h_new
+(x.grad and residual.grad are both the one dx), and a strided per-head view --
+with the parity bars: dx within one BF16 step of RNE_bf16(dx64), an FP32
+w.grad within the dw budget, a BF16 w.grad within the dw budget plus the
+half BF16 step of its own rounding.  The oracle takes its own rstd rounded to FP32, as in the
+parity tests.  Further GPU tests check that autograd gives exactly the bits
+of the C ABI entry points, in both modes; that a checkpointed step (forward,
+forward recompute, backward) gives the same gradient bits as the plain step;
+and that the cached workspace is reused, not reallocated.  The CPU tests
+check the names and that CPU tensors are rejected (there is no CPU path).
 """
+import numpy as np
 import pytest
 import torch
 import torch.utils.checkpoint as ckpt
 
 import cake_inputs
+import oracle
+from tests import tolerances as tol
 
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 
@@ -151,3 +159,88 @@ def test_caller_workspace(cake):
         grads.append((x.grad, w.grad))
     torch.cuda.synchronize()
     assert torch.equal(grads[0][0], grads[1][0]) and torch.equal(grads[0][1], grads[1][1])
+
+
+def _host_bits(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _oracle_grads(x, w, dy, eps, residual=None, dh=None):
+    """(dx64, dw64, rin, h rows, dy rows, dh rows) from the FP64 oracle for a
+    CPU case; rin is the oracle's rstd rounded to FP32."""
+    from tests.test_parity import oracle_bwd_inputs, rows_f64, view_of, wbits
+    T = x.shape[0]
+    nh = x.shape[1] if x.dim() == 3 else 1
+    H = x.shape[-1]
+    rin, hn = oracle_bwd_inputs(x, w, eps, residual)
+    h = torch.from_numpy(hn.view(np.int16)).view(torch.bfloat16).reshape(x.shape) if residual is not None else x
+    hv, dyv = view_of(h), view_of(dy)
+    dhv = view_of(dh) if dh is not None else None
+    dx64 = oracle.bwd_rows(T, nh, H, dyv, hv, rin, wbits(w), dh=dhv)
+    dw64 = oracle.dw_cols(T, nh, H, dyv, hv, rin)
+    return dx64, dw64, rin, rows_f64(h), rows_f64(dy), (rows_f64(dh) if dh is not None else None)
+
+
+def _check_grads(xgrad, wgrad, w, dx64, dw64, rin, hf, dyf, dhf):
+    H = w.numel()
+    rep = tol.dx_report(_host_bits(xgrad).reshape(-1, H), dx64, dyf, hf, w.double().numpy(), rin,
+                        oracle.bf16_round, oracle.bf16_bits_to_f64, dh=dhf)
+    assert rep["bounded"] == 0 and rep["off_cancellation"] == 0, rep
+    assert wgrad.dtype == w.dtype
+    if w.dtype == torch.float32:
+        assert float(tol.dw_budget_fraction(wgrad.cpu().numpy(), dw64).max()) <= 1.0
+    else:
+        # the FP32 dw within its budget, then rounded once to BF16
+        g = oracle.bf16_bits_to_f64(_host_bits(wgrad))
+        allow = tol.DW_ATOL + tol.DW_RTOL * np.abs(dw64) + tol.bf16_ulp(dw64) / 2
+        assert np.all(np.abs(g - dw64) <= allow)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("w_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("det", [True, False])
+def test_autograd_plain_against_oracle(cake, w_dtype, det):
+    c = cake_inputs.plain_case(257, 2048, w_dtype=w_dtype, seed=41)
+    dx64, dw64, rin, hf, dyf, _ = _oracle_grads(c["x"], c["w"], c["dy"], c["eps"])
+    x, w = _leaf(c["x"]), _leaf(c["w"])
+    cake.cake_rmsnorm(x, w, c["eps"], deterministic=det).backward(c["dy"].to(DEV))
+    torch.cuda.synchronize()
+    _check_grads(x.grad, w.grad, c["w"], dx64, dw64, rin, hf, dyf, None)
+
+
+@pytest.mark.gpu
+def test_autograd_residual_against_oracle(cake):
+    c = cake_inputs.residual_case(129, 6144, seed=42)
+    dx64, dw64, rin, hf, dyf, dhf = _oracle_grads(c["x"], c["w"], c["dy"], c["eps"], c["residual"], c["dh"])
+    x, res, w = _leaf(c["x"]), _leaf(c["residual"]), _leaf(c["w"])
+    y, h_new = cake.cake_rmsnorm(x, w, c["eps"], residual=res)
+    torch.autograd.backward([y, h_new], [c["dy"].to(DEV), c["dh"].to(DEV)])
+    torch.cuda.synchronize()
+    _check_grads(x.grad, w.grad, c["w"], dx64, dw64, rin, hf, dyf, dhf)
+    assert torch.equal(res.grad, x.grad)  # one dx is the gradient of both
+
+
+@pytest.mark.gpu
+def test_autograd_per_head_against_oracle(cake):
+    c = cake_inputs.heads_case(48, 24, strided=True, seed=43)
+    dx64, dw64, rin, hf, dyf, _ = _oracle_grads(c["x"], c["w"], c["dy"], c["eps"])
+    base, x = _leaf_view(c["x"])
+    w = _leaf(c["w"])
+    cake.cake_rmsnorm(x, w, c["eps"]).backward(c["dy"].to(DEV))
+    torch.cuda.synchronize()
+    g = base.grad.as_strided(x.shape, x.stride(), x.storage_offset())
+    _check_grads(g, w.grad, c["w"], dx64, dw64, rin, hf, dyf, None)
+
+
+@pytest.mark.gpu
+def test_backward_reuses_the_cached_workspace(cake):
+    from bwd_dw_column_gb300 import train
+    c = cake_inputs.plain_case(300, 1536, seed=44)
+    stream_key = (0, torch.cuda.current_stream().cuda_stream)
+    seen = []
+    for _ in range(3):
+        x, w = _leaf(c["x"]), _leaf(c["w"])
+        cake.cake_rmsnorm(x, w, c["eps"]).backward(c["dy"].to(DEV))
+        seen.append(train._ws_cache[stream_key].data_ptr())
+    torch.cuda.synchronize()
+    assert len(set(seen)) == 1
