@@ -366,17 +366,36 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
 // finalise behind the L2 atomics, or the grid barrier) add 4-27 us (T =
 // 32768 .. 131072, H = 256 .. 6144).  So both modes run the pair, whose dw
 // is also reproducible; CAKE_TUNE=form=N or force_single selects a single
-// kernel.  Per-thread accumulation: up to 2048 rows the plain FP32 sum (a
-// thread sums a handful of rows, far inside the budget); above, the blocked
-// form -- plain FP32 sums over 16 rows folded into a compensated pair whose
-// low parts live in shared memory -- which costs little more than the plain
-// sum (GB300, T = 32768 .. 65536: 1.5 - 8 % faster than Kahan's per-row
-// compensation) and keeps the worst dw element well inside the budget.
+// kernel.  Per-thread accumulation: the plain FP32 sum, the blocked form
+// (plain FP32 sums over 16 rows folded into a compensated pair whose low
+// parts live in shared memory, which costs little more than the plain sum),
+// Kahan, or TwoSum, by the accuracy windows below.
+//
+// Accuracy windows of the per-thread sums, by the rows each column sums
+// (T * nh): the cheapest form whose worst dw element stayed within 0.85 of
+// the budget (the pages' margin) over the accuracy protocol -- three input
+// families, x and dy ~ N(0, 1) -- on GB300:
+//   rows <= 2048       plain FP32 (a thread sums a handful of rows);
+//   rows <= 131072     blocked: 0.81 worst over 1440 inputs at H 4096 / 5120,
+//                      T 4096 .. 131072; 0.49 at 131072 rows of 256;
+//   rows <= 2^20       Kahan: blocked passes 0.85 beyond 131072 rows (0.88 at
+//                      T 262144, 1.15 at T 524288, 1.12 at 786432 rows of
+//                      256), Kahan stays at 0.32 - 0.39 up to 786432 rows;
+//   above              TwoSum (0.0006 at every measured size).
+// Costs against blocked, same shapes: Kahan 0.6 - 3 % (7 % at H 5120), TwoSum
+// 4 - 28 %.
 static void pick_variant(uint32_t rows, int deterministic, int &single, int &dwm)
 {
     (void)deterministic;
     single = kFormPair;
-    dwm = rows <= 2048 ? CAKE_DW_PLAIN : CAKE_DW_BLOCKED;
+    if (rows <= 2048)
+        dwm = CAKE_DW_PLAIN;
+    else if (rows <= 131072)
+        dwm = CAKE_DW_BLOCKED;
+    else if (rows <= (1u << 20))
+        dwm = CAKE_DW_KAHAN;
+    else
+        dwm = CAKE_DW_TWOSUM;
 }
 
 // Partial ranges per column per warp of the fixed-order reduce: about one

@@ -123,15 +123,17 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// A non-blocking test (no suspension): the cluster form's waits are short
+// and a suspended waiter on a remotely completed phase measured slow.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -146,7 +148,8 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait_cluster(bar, parity))
             return true;
-        if ((i & 3u) == 0 && globaltimer_ns() - t0 > limit_ns)
+        __nanosleep(32);
+        if ((i & 15u) == 0 && globaltimer_ns() - t0 > limit_ns)
             return false;
     }
 }

@@ -127,6 +127,19 @@ def test_forced_variants(cake):
     assert e.value.status == 1
 
 
+@pytest.mark.parametrize("shape,accum", [
+    ((1, 1, 1536), 0), ((2048, 1, 2048), 0),                 # plain FP32 sums
+    ((2049, 1, 2048), 1), ((131072, 1, 6144), 1),            # blocked
+    ((32768, 4, 256), 1),                                    # 131072 rows of the per-head view
+    ((131073, 1, 4096), 3), ((32768, 24, 256), 3),           # Kahan past the blocked window
+    ((1 << 20, 1, 256), 3), (((1 << 20) + 1, 1, 256), 2),    # TwoSum beyond
+])
+def test_accuracy_windows(cake, shape, accum):
+    # the per-thread dw sums the table takes by the rows each column sums
+    for det in (True, False):
+        assert cake.cake_rmsnorm_bwd_select(shape, deterministic=det)["dw_accum"] == accum
+
+
 @pytest.mark.parametrize("shape,status", [
     ((10, 1, 12), 2),          # H not a multiple of 8
     ((10, 1, 8200), 2),        # H above the maximum

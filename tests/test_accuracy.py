@@ -10,10 +10,11 @@ window within 0.85 up to T 65536).  dw does not depend on w, so one weight
 stands for both dtypes.
 
 * ``test_dw_accuracy_hard_points`` (part of the GPU suite): the sweep's
-  largest T points, 44032 and 131072, both widths, every family, one seed:
-  the window table's choice in both modes and the forced atomic single
-  kernel, every column against the oracle; the table's choice must stay
-  within 0.85 of the budget and every form within the budget.
+  largest T points, 44032 and 131072, both widths, and 786432 rows of 256
+  (past the blocked window), every family, one seed: the window table's
+  choice in both modes and the forced atomic single kernel, every column
+  against the oracle; the table's choice must stay within 0.85 of the budget
+  and every form within the budget.
 * ``test_dw_accuracy_sweep`` (slow; runs when CAKE_SWEEP_SEEDS is set): the
   whole protocol with that many seeds per family over every accumulation
   form, the torch FP32 eager column sum beside them as the pages' comparator;
@@ -117,6 +118,9 @@ def run_cases(cake, cases, forms, eager=False, jobs=None):
 def test_dw_accuracy_hard_points(cake):
     forms = TABLE_FORMS + [("atomic_table_accum", 1, None, False)]
     cases = [(H, T, f, 0) for H in cake_inputs.SWEEP_H for T in (44032, 131072) for f in cake_inputs.SWEEP_FAMILIES]
+    # past the blocked window: 786432 rows of 256 (the dw of the per-head
+    # [32768, 24, 256] view), where the table takes Kahan sums
+    cases += [(256, 786432, f, 0) for f in cake_inputs.SWEEP_FAMILIES]
     scores = run_cases(cake, cases, forms, jobs=4)
     worst = {n: max(s[n] for s in scores) for n, *_ in forms}
     for (H, T, f, _), s in zip(cases, scores):
