@@ -181,7 +181,8 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 _UNITS = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
-          "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0}
+          "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0,
+          "ns": 1e-9, "us": 1e-6, "ms": 1e-3, "s": 1.0}
 
 
 def parse_ncu_csv(path: str, kernel: str):

@@ -88,6 +88,15 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     // faster over a whole T = 65536 step, although it costs up to 3 us more
     // at small T)
     stage_weight<VPT != 1>(s, L, p.w, p.w_f32);
+    // with 8 columns per thread a thread's columns are the same on every row:
+    // keep their weights in registers instead of reading shared memory per
+    // row (GB300: 3 % off the main kernel for rows of 256 and 640 with plain
+    // or blocked sums; the Kahan and TwoSum builds would spill, so they keep
+    // reading shared memory)
+    constexpr bool kWreg = VPT == 1 && (DWM == CAKE_DWM_PLAIN || DWM == CAKE_DWM_BLOCKED);
+    float2 wreg[4];
+    if constexpr (kWreg)
+        weight_pairs(s, L, gtid < nvec ? gtid : 0, wreg);
 
     // dw accumulators for this thread's columns (pairs of adjacent columns):
     // the partial is hi + lo in every form.
@@ -214,7 +223,13 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                         dr = dys[v];
                     }
                     float2 w2[4];
-                    weight_pairs(s, L, v < nvec ? v : 0, w2);
+                    if constexpr (kWreg) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            w2[q] = wreg[q];
+                    } else {
+                        weight_pairs(s, L, v < nvec ? v : 0, w2);
+                    }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float2 xv = bf2(word(xr, q));

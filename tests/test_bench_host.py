@@ -103,7 +103,7 @@ NCU_CSV = """==PROF== Connected to process 1
 "1","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","usecond","200"
 "2","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Mbyte","801.5"
 "2","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","Mbyte","400.75"
-"2","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","usecond","202"
+"2","1","python","h","void cake::bwd_rows_kernel<4, 1, 0, 0>(cake::BwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","ns","202000"
 """
 
 

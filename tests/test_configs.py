@@ -166,9 +166,44 @@ def test_per_head(cake, name):
     run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], name=name)
 
 
-@pytest.mark.parametrize("name", ["h4096_t65536_sweep", "h5120_t65536_sweep"])
+@pytest.mark.parametrize("name", ["h4096_t65536_sweep", "h5120_t65536_sweep", "h4096_t44032_sweep",
+                                  "h5120_t131072_sweep", "h4096_t131072_sweep"])
 def test_sweep_widths(cake, name):
-    # the accuracy sweep's widths at T = 65536: two rows per group (H = 4096)
-    # and 24 columns per thread (H = 5120); dx of sampled rows, dw of every column
+    # the accuracy sweep's widths at its large T: 32 columns per thread (H =
+    # 4096) and 24 (H = 5120); dx of sampled rows, dw of every column
     c = cake_inputs.make(name, seed=0, device=DEV)
     run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], full_dx=False, name=name)
+
+
+@pytest.mark.parametrize("T,H", [(65536, 2048), (32768, 4096), (20000, 512)])
+def test_single_kernel_forms_at_size(cake, T, H):
+    """Every one-kernel form -- FP64 atomics, the tree, the cooperative grid
+    and the cluster form -- at tens of thousands of rows, with the table's
+    accumulation: dw of every column against the oracle, dx the same bits as
+    the pair's (forms the layout does not offer are skipped)."""
+    c = cake_inputs.plain_case(T, H, family="outlier", w_dtype=torch.float32, seed=T + H, device=DEV)
+    x, dy, w = c["x"], c["dy"], c["w"]
+    xv, dyv = host_view(x), host_view(dy)
+    _, r64, _ = oracle.fwd_rows(T, 1, H, xv, wbits(w), c["eps"], want_y=False, want_h=False)
+    rin = r64.astype(np.float32)
+    dw64 = oracle.dw_cols(T, 1, H, dyv, xv, rin)
+    r_d = torch.from_numpy(rin).to(DEV)
+    ws = cake.cake_rmsnorm_bwd_workspace(x, w.dtype, deterministic=False)
+    ref_dx, _ = cake.cake_rmsnorm_bwd(dy, x, r_d, w, deterministic=True, workspace=ws)
+    torch.cuda.synchronize()
+    ref_bits = bits(ref_dx)
+    worst = {}
+    for form in (1, 2, 3, 4):
+        try:
+            dx, dw = cake.cake_rmsnorm_bwd_forced(dy, x, r_d, w, deterministic=form != 1, force_single=form,
+                                                  workspace=ws)
+        except cake.CakeError as e:
+            assert form == 2 and e.status == 2  # the tree form needs 8 columns per thread
+            continue
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(dx), ref_bits)
+        worst[form] = float(tol.dw_budget_fraction(dw.cpu().numpy(), dw64).max())
+        assert worst[form] <= 1.0, worst
+        del dx, dw
+    report.record(f"one-kernel forms T={T} H={H}", dw_worst=max(worst.values()),
+                  **{f"form{k}": round(v, 4) for k, v in worst.items()})
