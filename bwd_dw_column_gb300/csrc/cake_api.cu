@@ -55,19 +55,22 @@ constexpr size_t kSmemPerSM = 220 * 1024; // budget for the rings of co-resident
 constexpr int kMaxStages = 16;
 // CTAs in the cluster form's one cluster (the portable maximum).
 constexpr int kClusterCTAs = 8;
+// Backward row sets of at most this many elements (rows * H) run as one CTA.
+constexpr int64_t kOneCtaElems = 24576;
 
 enum Kind { kFwd = 0, kBwd = 1 };
 
 // Developer override of the table, for tuning sweeps: CAKE_TUNE holds
 // comma-separated key=value pairs among vpt, groups, cps, stages, rpg, form,
-// cluster (backward) and fvpt, fgroups, fcps, fstages (forward).  Unset, the
-// table below rules.
+// cluster, onecta (backward) and fvpt, fgroups, fcps, fstages (forward).
+// Unset, the table below rules.
 // A different row layout (vpt) changes the reduction order and therefore the
 // bits of dx / y / rstd; a different cps or groups changes the pair's
 // partition and therefore the bits of the deterministic dw.
 struct Tune {
     int v[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages, rpg, form+1]
     int cluster = 0;                                         // cluster form: CTAs per cluster
+    int one_cta_elems = 0;                                   // backward: one CTA up to rows * H elements
 };
 
 static Tune parse_tune(const char *t)
@@ -90,6 +93,8 @@ static Tune parse_tune(const char *t)
                     r.v[k][i] = i == 5 ? val + 1 : val;
         if (klen == 7 && strncmp(p, "cluster", 7) == 0 && val >= 1 && val <= kMaxCluster)
             r.cluster = val;
+        if (klen == 6 && strncmp(p, "onecta", 6) == 0 && val >= 0)
+            r.one_cta_elems = val;
         const char *comma = strchr(eq, ',');
         if (!comma)
             break;
@@ -337,6 +342,14 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     uint32_t ctas = rows == 0 ? 0 : (rows + tile - 1) / tile; // at least one tile per CTA
     if (ctas > max_ctas)
         ctas = max_ctas;
+    // backward over a few rows: one CTA, whose partial is dw, so the pair is
+    // a single launch (GB300, event-timed: H = 256 T = 16 8.3 us against
+    // 10.2 us for two CTAs and the reduce; H = 4096 T = 4 10.5 against 12.3;
+    // H = 6144 T = 4 11.8 against 13.1; even at H = 1536 T = 16 and H = 256
+    // T = 64, slower beyond: one SM cannot stream more rows in time)
+    const int64_t one_cta = tune().one_cta_elems > 0 ? tune().one_cta_elems : kOneCtaElems;
+    if (kind == kBwd && ctas > 1 && (int64_t)rows * H <= one_cta)
+        ctas = 1;
     p.rows_per_cta = ctas ? (rows + ctas - 1) / ctas : 0;
     p.ctas = p.rows_per_cta ? (int)((rows + p.rows_per_cta - 1) / p.rows_per_cta) : 0;
     p.single = single;
@@ -698,8 +711,11 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     p.wait_ns = wait_ns;
     p.grid_extra = grid_extra;
     p.cluster = plan.single == kFormCluster ? plan.ctas : 0;
+    // a pair of one CTA writes dw from the main kernel (same bits as the
+    // reduce of its single partial); the separate halves keep the partial
+    p.direct_dw = plan.single == kFormPair && plan.ctas == 1 && phase == kWhole;
     cudaError_t e = launch_bwd_rows(p, plan.rl.vpt, plan.single, plan.dwm, plan.ctas, plan.smem, s);
-    if (e != cudaSuccess || plan.single != kFormPair || phase == kMainOnly)
+    if (e != cudaSuccess || plan.single != kFormPair || phase == kMainOnly || p.direct_dw)
         return cuda_status(e);
     ReduceParams rp{p.partials, plan.ctas, H, dw, reduce_slices(H, plan.ctas)};
     return cuda_status(launch_dw_reduce(rp, s));

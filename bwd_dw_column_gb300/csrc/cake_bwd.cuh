@@ -461,6 +461,30 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         return;
     }
 
+    if constexpr (FORM == kFormPair) {
+        if (p.direct_dw) {
+            // a pair of one CTA: its partial is dw (the reduce of a single
+            // partial would give the same bits, hi + lo rounded once)
+            if (gid == 0) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = k * 32 * W + gtid;
+                    if (v < nvec) {
+                        float o[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            o[2 * q] = __fadd_rn(hi[k][q].x, lo[k][q].x);
+                            o[2 * q + 1] = __fadd_rn(hi[k][q].y, lo[k][q].y);
+                        }
+                        float4 *d4 = reinterpret_cast<float4 *>(p.dw) + 2 * v;
+                        d4[0] = make_float4(o[0], o[1], o[2], o[3]);
+                        d4[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            }
+            return;
+        }
+    }
     if (FORM != kFormAtomic) {
         if (gid == 0) {
             float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);

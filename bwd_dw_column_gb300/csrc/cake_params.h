@@ -134,6 +134,7 @@ struct BwdParams {
     int grid_extra;     // grid form: arrivals its barrier expects beyond the CTA count (0; the
                         // timeout test sets 1 so that the barrier never completes)
     int cluster;        // cluster form: CTAs in the (one) cluster, which is the whole grid
+    int direct_dw;      // pair of one CTA: the main kernel writes dw itself (no reduce launch)
 };
 
 struct ReduceParams {

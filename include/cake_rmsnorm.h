@@ -143,8 +143,10 @@ cake_status cake_rmsnorm_bwd_workspace_init(void *workspace, size_t workspace_by
  * table may pick a single-kernel form where one is faster than the pair, and
  * dw is then not guaranteed bitwise reproducible; on GB300 none is faster at
  * any measured shape, so the table runs the pair in both modes
- * (cake_rmsnorm_bwd_forced selects a single kernel).  dx is the same bits in
- * every mode and variant.  T = 0: dw is zero-filled and CAKE_OK returned.
+ * (cake_rmsnorm_bwd_forced selects a single kernel).  A row set of at most
+ * 24576 elements (T * nh * H) runs as one CTA whose main kernel writes dw
+ * itself: one launch in both modes.  dx is the same bits in every mode and
+ * variant.  T = 0: dw is zero-filled and CAKE_OK returned.
  */
 cake_status cake_rmsnorm_bwd(const cake_shape *shape, const cake_tensor *dy,
                              const cake_tensor *x, const float *rstd, const void *w,

@@ -108,6 +108,17 @@ def test_row_layout_depends_on_h_alone(cake):
         assert len(layouts) == 1, (H, layouts)
 
 
+@pytest.mark.parametrize("shape,one", [((1, 1, 1536), True), ((16, 1, 1536), True), ((17, 1, 1536), False),
+                                       ((96, 1, 256), True), ((97, 1, 256), False), ((4, 24, 256), True),
+                                       ((4, 1, 6144), True), ((5, 1, 6144), False)])
+def test_small_row_sets_run_as_one_cta(cake, shape, one):
+    # up to 24576 elements the pair is one CTA whose main kernel writes dw
+    # (one launch); beyond, several CTAs and the fixed-order reduce
+    for det in (True, False):
+        v = cake.cake_rmsnorm_bwd_select(shape, deterministic=det)
+        assert (v["ctas"] == 1) == one, (shape, v)
+
+
 def test_partition_depends_on_shape_alone(cake):
     a = cake.cake_rmsnorm_bwd_select((65536, 1, 2048), deterministic=True)
     b = cake.cake_rmsnorm_bwd_select((65536, 1, 2048), deterministic=True)
