@@ -148,13 +148,36 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Host-only source: argument validation, the window table and launch dispatch.
+# It decides the launch plan, which a traffic record stores and compares
+# itself; every other file under csrc/ is device code or shared by it.
+HOST_ONLY_SOURCES = ("cake_api.cu",)
+
+
 def kernel_source_hash():
+    """Hash of the kernel sources (every csrc file but the host-only ones)."""
     csrc = os.path.join(ROOT, "bwd_dw_column_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
+        if f in HOST_ONLY_SOURCES:
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
+
+
+def workload_plan(workload: str):
+    """The backward plan (the window table's variant) of a workload's main
+    kernel, as the library picks it now; None without the library."""
+    try:
+        import bwd_dw_column_gb300 as cake
+        import cake_inputs
+        spec = cake_inputs.WORKLOADS[workload]
+        shape = (spec["T"], spec.get("heads", 1), spec.get("H", 256))
+        return cake.cake_rmsnorm_bwd_select(shape, spec["w_dtype"], deterministic=True,
+                                            has_dh=spec["kind"] == "res")
+    except Exception:
+        return None
 
 
 def traffic_json():
@@ -163,7 +186,8 @@ def traffic_json():
 
 def traffic_record(kernel: str, workload: str):
     """The committed ncu record (DRAM bytes per launch, the summary file) when
-    its counters were taken on the current kernel sources; else None."""
+    its counters were taken on the current kernel sources and with the launch
+    plan the table picks now; else None."""
     try:
         with open(traffic_json()) as f:
             rec = json.load(f)
@@ -171,6 +195,8 @@ def traffic_record(kernel: str, workload: str):
         return None
     ent = rec.get(f"{kernel}:{workload}")
     if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    if "plan" in ent and ent["plan"] != workload_plan(workload):
         return None
     return ent
 
@@ -229,6 +255,7 @@ def record_traffic(args):
         rec = {}
     rec[f"{args.kernel}:{args.workload}"] = {
         "source_hash": here,
+        "plan": workload_plan(args.workload),
         "dram_bytes_per_launch": int(round(statistics.mean(per) * args.scale)),
         "launches": len(per),
         "ncu_us_per_launch": round(statistics.mean(dur) * 1e6 * args.scale, 2) if dur else None,

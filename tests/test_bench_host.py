@@ -95,6 +95,30 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.traffic_record("bwd_rows_kernel", "missing") is None
 
 
+def test_traffic_record_follows_the_launch_plan(tmp_path, monkeypatch):
+    # a record also holds the plan its counters were taken with: a table
+    # change that gives the workload another launch makes it stale
+    import bench
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles").mkdir()
+    rec = {"bwd_rows_kernel:w": {"source_hash": h, "dram_bytes_per_launch": 5, "plan": {"ctas": 152}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    monkeypatch.setattr(bench, "workload_plan", lambda w: {"ctas": 152})
+    assert bench.recorded_traffic("bwd_rows_kernel", "w") == 5
+    monkeypatch.setattr(bench, "workload_plan", lambda w: {"ctas": 304})
+    assert bench.recorded_traffic("bwd_rows_kernel", "w") is None
+
+
+def test_kernel_hash_leaves_out_the_host_only_source():
+    import bench
+    csrc = os.path.join(ROOT, "bwd_dw_column_gb300", "csrc")
+    files = sorted(os.listdir(csrc))
+    assert "cake_api.cu" in files and bench.HOST_ONLY_SOURCES == ("cake_api.cu",)
+    assert any(f.startswith("cake_bwd") for f in files)
+
+
 NCU_CSV = """==PROF== Connected to process 1
 "ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"
 "0","1","python","h","void cake::fwd_rows_kernel<3>(cake::FwdParams)","1","7","(416, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Gbyte","9.99"
