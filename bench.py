@@ -14,9 +14,10 @@ and the accuracy sweep's shapes H in {4096, 5120} x T in {4096, 44032, 65536,
 
   value         achieved GB/s = algorithmic bytes of the step / its device
                 time (inputs resident in HBM, L2 flushed before every step)
-  e2e           the same metric through the C ABI from pinned host buffers:
-                the host->device copies of the step's inputs and the
-                device->host copies of dx and dw are inside the timed region
+  e2e           the same metric through the C ABI entry point that takes host
+                buffers: every step copies its inputs from page-locked host
+                memory and dx and dw back, in row chunks whose copies and
+                kernels overlap, all inside the timed region
   roofline      the main kernel alone, timed with CUDA events on its stream,
                 against the measured HBM copy bandwidth
   cpu_baseline  the FP64 CPU oracle on a bounded sample of the same workload
@@ -92,6 +93,8 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="with --profile: the workload's shape at this many tokens (a smaller case for ncu)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=16,
+                    help="row chunks of the end-to-end step (copies and kernels overlap across chunks)")
     ap.add_argument("--profile", choices=["det", "nondet", "fwd", "main", "single_atomic", "single_grid",
                                           "single_cluster", "all"], default=None,
                     help="run only the named loop(s) with few launches (for ncu); prints per-call times")
@@ -505,35 +508,23 @@ def short_variant(v):
                               "rows_per_group", "stages", "ctas")}
 
 
-def e2e_loop(cake, torch, wl: Workload, K, Wm, flush, stream, dev, det):
-    """The backward through the public entry point from pinned host buffers:
-    every step copies its inputs in and dx, dw out (all inside the timed region)."""
-    def host(t):
-        if t is None:
-            return None
-        if not t.is_contiguous():  # a strided view travels as its whole buffer
-            t = t.as_strided((t.untyped_storage().nbytes() // t.element_size(),), (1,), 0)
-        return t.cpu().pin_memory()
-
-    h, dy, dh, rstd, w, dx = wl.h, wl.dy, wl.dh, wl.rstd, wl.w, wl.dx
-    hx, hdy, hdh, hrstd, hw = (host(t) for t in (h, dy, dh, rstd, w))
-    hdx = torch.empty(dx.shape, dtype=torch.bfloat16).pin_memory()
+def e2e_loop(cake, torch, wl: Workload, K, Wm, flush, stream, dev, det, chunks):
+    """The backward through the public entry point that takes host buffers
+    (cake_rmsnorm_bwd_host): every step copies the inputs from page-locked
+    host memory to the device and dx and dw back, inside the call, in row
+    chunks whose copies and kernels overlap.  A strided view travels as its
+    dense rows (gathered on the host once, outside the timed region)."""
+    pin = lambda t: None if t is None else t.contiguous().cpu().pin_memory()
+    hx, hdy, hdh, hrstd, hw = (pin(t) for t in (wl.h, wl.dy, wl.dh, wl.rstd, wl.w))
+    hdx = torch.empty(hx.shape, dtype=torch.bfloat16).pin_memory()
     hdw = torch.empty(wl.H, dtype=torch.float32).pin_memory()
-    bx = torch.empty(hx.shape, dtype=hx.dtype, device=dev)
-    x2 = bx if h.is_contiguous() else bx.as_strided(h.shape, h.stride(), h.storage_offset())
-    dy2, r2, w2, dx2 = (torch.empty_like(t) for t in (dy, rstd, w, dx))
-    dh2 = torch.empty_like(dh) if dh is not None else None
+    n = cake.cake_rmsnorm_bwd_host_staging_size((wl.T, wl.nh, wl.H), wl.w.dtype, has_dh=wl.dh is not None,
+                                                chunks=chunks)
+    staging = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
 
     def step():
-        bx.copy_(hx, non_blocking=True)
-        dy2.copy_(hdy, non_blocking=True)
-        if dh2 is not None:
-            dh2.copy_(hdh, non_blocking=True)
-        r2.copy_(hrstd, non_blocking=True)
-        w2.copy_(hw, non_blocking=True)
-        cake.cake_rmsnorm_bwd(dy2, x2, r2, w2, dh2, deterministic=det, workspace=wl.ws, dx=dx2, dw=wl.dw)
-        hdx.copy_(dx2, non_blocking=True)
-        hdw.copy_(wl.dw, non_blocking=True)
+        cake.cake_rmsnorm_bwd_host(hdy, hx, hrstd, hw, hdh, dx=hdx, dw=hdw, staging=staging, chunks=chunks,
+                                   deterministic=det)
 
     times = time_loop(torch, step, K, Wm, flush, stream)
     h2d = sum(t.numel() * t.element_size() for t in (hx, hdy, hdh, hrstd, hw) if t is not None)
@@ -597,8 +588,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks = clk.summary()
 
-    t_e2e, h2d, d2h = e2e_loop(cake, torch, wl, K, Wm, flush, stream, dev, det=False)
-    launches += 2 * K
+    t_e2e, h2d, d2h = e2e_loop(cake, torch, wl, K, Wm, flush, stream, dev, det=False, chunks=args.e2e_chunks)
+    e2e_chunks = min(args.e2e_chunks, wl.R)
+    launches += (e2e_chunks + 1) * K
     assert cake.cake_rmsnorm_device_status() == 0
     tot_e2e, mean_e2e = aggregate_times(t_e2e, world, dev)
 
@@ -662,6 +654,8 @@ def run_ours(args):
             "ms_per_step": round(mean_e2e, 4),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+            "entry_point": "cake_rmsnorm_bwd_host (page-locked host buffers in and out, "
+                           f"{e2e_chunks} row chunks whose copies and kernels overlap)",
         },
         "gpu_launches": launches,
         "clocks": clocks,

@@ -32,7 +32,8 @@ __all__ = [
     "CakeError", "load_library", "cake_rmsnorm_fwd", "cake_rmsnorm_bwd", "cake_rmsnorm_bwd_forced",
     "cake_rmsnorm_bwd_main", "cake_rmsnorm_bwd_reduce", "cake_rmsnorm_bwd_noalloc",
     "cake_rmsnorm_bwd_workspace_size", "cake_rmsnorm_bwd_workspace", "cake_rmsnorm_bwd_workspace_init",
-    "cake_rmsnorm_bwd_select", "cake_rmsnorm_bwd_timeout_test",
+    "cake_rmsnorm_bwd_select", "cake_rmsnorm_bwd_timeout_test", "cake_rmsnorm_bwd_host",
+    "cake_rmsnorm_bwd_host_staging_size",
     "cake_rmsnorm_device_status", "cake_status_str", "cake_rmsnorm_plan_occupancy", "LIB_PATH", "DW_PLAIN", "DW_BLOCKED", "DW_TWOSUM", "DW_KAHAN",
 ]
 
@@ -106,6 +107,11 @@ def load_library(path: str = LIB_PATH):
         lib.cake_rmsnorm_bwd_noalloc.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_noalloc.argtypes = [_P(_Shape), _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_int,
                                                  _P(_Tensor), _P(_Tensor), _vp, _vp]
+        lib.cake_rmsnorm_bwd_host_staging_size.restype = ctypes.c_size_t
+        lib.cake_rmsnorm_bwd_host_staging_size.argtypes = [_P(_Shape), ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.cake_rmsnorm_bwd_host.restype = ctypes.c_int
+        lib.cake_rmsnorm_bwd_host.argtypes = [_P(_Shape), _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                              ctypes.c_size_t, ctypes.c_int, ctypes.c_int, _vp]
         lib.cake_rmsnorm_bwd_timeout_test.restype = ctypes.c_int
         lib.cake_rmsnorm_bwd_timeout_test.argtypes = [_P(_Shape), _P(_Tensor), _P(_Tensor), _vp, _vp, ctypes.c_int,
                                                       _P(_Tensor), _vp, _vp, ctypes.c_size_t, ctypes.c_uint32, _vp]
@@ -345,6 +351,56 @@ def cake_rmsnorm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, rstd: torch.Tens
                                       ctypes.byref(_tensor(dh)) if dh is not None else None,
                                       ctypes.byref(_tensor(dx)), ctypes.c_void_p(dw.data_ptr()), _stream(stream))
     _check(st, "cake_rmsnorm_bwd_noalloc")
+    return dx, dw
+
+
+def cake_rmsnorm_bwd_host_staging_size(x_or_shape, w_dtype=torch.bfloat16, has_dh: bool = False,
+                                       chunks: int = 8) -> int:
+    """Device staging bytes cake_rmsnorm_bwd_host needs for this row set."""
+    lib = load_library()
+    shape = _shape(x_or_shape) if isinstance(x_or_shape, torch.Tensor) else _Shape(*x_or_shape)
+    wd = CAKE_FP32 if w_dtype in (torch.float32, CAKE_FP32) else CAKE_BF16
+    return int(lib.cake_rmsnorm_bwd_host_staging_size(ctypes.byref(shape), wd, int(bool(has_dh)), int(chunks)))
+
+
+def _host_rows(t: torch.Tensor, what: str, dtype) -> torch.Tensor:
+    if t.is_cuda:
+        raise ValueError(f"{what} is a host tensor here")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous (dense rows)")
+    return t
+
+
+def cake_rmsnorm_bwd_host(dy: torch.Tensor, x: torch.Tensor, rstd: torch.Tensor, w: torch.Tensor,
+                          dh: torch.Tensor | None = None, *, dx: torch.Tensor, dw: torch.Tensor,
+                          staging: torch.Tensor, chunks: int = 8, deterministic: bool = True, stream=None):
+    """Backward over host (CPU, preferably pinned) tensors: the chunked copies and
+    kernels overlap on the device.  dx and dw are host tensors written once the
+    stream reaches the end of the call; staging is a device uint8 tensor of
+    cake_rmsnorm_bwd_host_staging_size bytes."""
+    lib = load_library()
+    for t, n in ((dy, "dy"), (x, "x"), (dh, "dh"), (dx, "dx")):
+        if t is not None:
+            _host_rows(t, n, torch.bfloat16)
+            _same_rows(x, t, n)
+    _host_rows(rstd, "rstd", torch.float32)
+    _host_rows(dw, "dw", torch.float32)
+    if w.is_cuda or not w.is_contiguous():
+        raise ValueError("w is a contiguous host tensor here")
+    _need_cuda(staging)
+    T, nh, H, _, _ = _rows_of(x)
+    if rstd.numel() != T * nh or dw.numel() != H:
+        raise ValueError("rstd must hold T*nh and dw H elements")
+    shape = _shape(x)
+    st = lib.cake_rmsnorm_bwd_host(ctypes.byref(shape), ctypes.c_void_p(dy.data_ptr()), ctypes.c_void_p(x.data_ptr()),
+                                   ctypes.c_void_p(rstd.data_ptr()), ctypes.c_void_p(w.data_ptr()), _w_dtype(w),
+                                   ctypes.c_void_p(dh.data_ptr()) if dh is not None else None,
+                                   ctypes.c_void_p(dx.data_ptr()), ctypes.c_void_p(dw.data_ptr()),
+                                   ctypes.c_void_p(staging.data_ptr()), staging.numel() * staging.element_size(),
+                                   int(chunks), int(bool(deterministic)), _stream(stream))
+    _check(st, "cake_rmsnorm_bwd_host")
     return dx, dw
 
 

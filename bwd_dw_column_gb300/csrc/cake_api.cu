@@ -721,6 +721,232 @@ cake_status run_bwd(const cake_shape *shape, const cake_tensor *dy, const cake_t
     return cuda_status(launch_dw_reduce(rp, s));
 }
 
+// ------------------------------------------------------- from host buffers
+//
+// The backward over rows that live in host memory: the rows go in chunks, and
+// the copy of chunk c + 1 to the device, the main kernel of chunk c and the
+// copy of chunk c - 1's dx back overlap on three streams (the caller's for the
+// kernels, two of the library's for the copies).  Every chunk's CTA partials
+// stay in the staging memory and one fixed-order reduce over all of them gives
+// dw, so dw is reproducible for a given shape and chunk count.
+
+constexpr int kHostSlots = 3;       // staging slots the chunks rotate through
+constexpr int kHostMaxChunks = 64;
+constexpr int kHostMaxDevices = 64;
+
+struct HostChunking {
+    int chunks, slots;
+    uint32_t rows_c, rows_last;  // rows of a full chunk and of the last one
+    Plan full, last;
+    size_t off_x, off_dy, off_dh, off_rstd, off_dx, slot_bytes; // within a slot
+    size_t off_w, off_dw, off_part, total;
+};
+
+bool host_chunking(int H, uint32_t rows, int has_dh, int w_elem_bytes, int chunks, HostChunking *c)
+{
+    if (chunks < 1 || chunks > kHostMaxChunks || rows == 0)
+        return false;
+    const uint32_t k = (uint32_t)chunks < rows ? (uint32_t)chunks : rows;
+    c->rows_c = (rows + k - 1) / k;
+    c->chunks = (int)((rows + c->rows_c - 1) / c->rows_c); // every chunk holds rows
+    c->rows_last = rows - (uint32_t)(c->chunks - 1) * c->rows_c;
+    c->slots = c->chunks < kHostSlots ? c->chunks : kHostSlots;
+    // the accumulation form follows the rows every column sums in all
+    int single, dwm;
+    pick_variant(rows, 1, single, dwm);
+    const int ntens = has_dh ? 3 : 2;
+    c->full = make_plan(H, c->rows_c, ntens, kBwd, kFormPair, dwm);
+    c->last = make_plan(H, c->rows_last, ntens, kBwd, kFormPair, dwm);
+    const size_t act = align256((size_t)c->rows_c * H * 2);
+    c->off_x = 0;
+    c->off_dy = act;
+    c->off_dh = 2 * act;
+    c->off_rstd = (has_dh ? 3 : 2) * act;
+    c->off_dx = c->off_rstd + align256((size_t)c->rows_c * 4);
+    c->slot_bytes = c->off_dx + act;
+    c->off_w = (size_t)c->slots * c->slot_bytes;
+    c->off_dw = c->off_w + align256((size_t)H * w_elem_bytes);
+    c->off_part = c->off_dw + align256((size_t)H * 4);
+    c->total = c->off_part + (size_t)c->chunks * c->full.ctas * H * 8;
+    return true;
+}
+
+// The library's two copy streams and the events that order the chunks, per
+// device, created at the first call on that device and kept.
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t in_ready[kHostSlots] = {}, computed[kHostSlots] = {}, out_done[kHostSlots] = {};
+    std::mutex mu; // one enqueue at a time per device
+    bool ready = false;
+};
+
+HostStreams g_host_streams[kHostMaxDevices];
+std::mutex g_host_init_mu;
+
+cudaError_t host_streams(int dev, HostStreams **out)
+{
+    if (dev < 0 || dev >= kHostMaxDevices)
+        return cudaErrorInvalidDevice;
+    HostStreams &h = g_host_streams[dev];
+    std::lock_guard<std::mutex> g(g_host_init_mu);
+    if (!h.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking);
+        cudaEvent_t *evs[] = {&h.start, &h.end};
+        for (cudaEvent_t *ev : evs)
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        for (int i = 0; i < kHostSlots && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&h.in_ready[i], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&h.computed[i], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&h.out_done[i], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess)
+            return e;
+        h.ready = true;
+    }
+    *out = &h;
+    return cudaSuccess;
+}
+
+// One chunk's main kernel: rows [0, rows) of a dense staging slot, its CTA
+// partials at `partials`.
+cudaError_t launch_chunk_main(const Plan &plan, int H, uint32_t rows, int has_dh, const uint16_t *x,
+                              const uint16_t *dy, const uint16_t *dh, const float *rstd, const void *w,
+                              int w_f32, uint16_t *dx, float *dw, float2 *partials, cudaStream_t s)
+{
+    const cake_shape shape{rows, 1, H};
+    BwdParams p{};
+    p.L = make_layout(plan, H, rows, 1, has_dh ? 3 : 2);
+    const cake_tensor tx{const_cast<uint16_t *>(x), H, 0}, tdy{const_cast<uint16_t *>(dy), H, 0},
+        tdh{const_cast<uint16_t *>(dh), H, 0}, tdx{dx, H, 0};
+    p.x = make_view(&tx, &shape);
+    p.dy = make_view(&tdy, &shape);
+    p.dh = make_view(has_dh ? &tdh : nullptr, &shape);
+    p.rstd = rstd;
+    p.w = w;
+    p.w_f32 = w_f32;
+    const RowView dxv = make_view(&tdx, &shape);
+    p.dx = dx;
+    p.dx_st = dxv.st;
+    p.dx_sh = dxv.sh;
+    p.dx_row_stride = dxv.row_stride;
+    p.dx_uniform = dxv.uniform;
+    p.dw = dw;
+    p.partials = partials;
+    p.banks = 1;
+    p.block_rows = 16;
+    p.status = nullptr;
+    p.wait_ns = kWaitLimitNs;
+    return launch_bwd_rows(p, plan.rl.vpt, kFormPair, plan.dwm, plan.ctas, plan.smem, s);
+}
+
+cake_status run_bwd_host(const cake_shape *shape, const void *dy, const void *x, const float *rstd,
+                         const void *w, cake_dtype w_dtype, const void *dh, void *dx, float *dw, void *staging,
+                         size_t staging_bytes, int chunks, cake_stream_t stream)
+{
+    uint32_t rows = 0;
+    cake_status st = check_shape(shape, &rows);
+    if (st != CAKE_OK)
+        return st;
+    if (w_dtype != CAKE_BF16 && w_dtype != CAKE_FP32)
+        return CAKE_ERR_INVALID;
+    if (chunks < 1 || chunks > kHostMaxChunks || !w || !dw)
+        return CAKE_ERR_INVALID;
+    const int H = (int)shape->hidden;
+    if (rows == 0) {
+        std::memset(dw, 0, (size_t)H * sizeof(float)); // nothing to copy: dw is zero now
+        return CAKE_OK;
+    }
+    if (!dy || !x || !rstd || !dx)
+        return CAKE_ERR_INVALID;
+    const int has_dh = dh != nullptr;
+    const int wb = w_dtype == CAKE_FP32 ? 4 : 2;
+    HostChunking c;
+    if (!host_chunking(H, rows, has_dh, wb, chunks, &c))
+        return CAKE_ERR_INVALID;
+    if (!staging || staging_bytes < c.total)
+        return CAKE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(staging) & 255u) != 0)
+        return CAKE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = -1, sdev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess)
+        return CAKE_ERR_CUDA;
+    if (sdev != dev)
+        return CAKE_ERR_INVALID;
+    HostStreams *hs = nullptr;
+    if (host_streams(dev, &hs) != cudaSuccess)
+        return CAKE_ERR_CUDA;
+    std::lock_guard<std::mutex> g(hs->mu);
+
+    uint8_t *base = static_cast<uint8_t *>(staging);
+    float2 *part = reinterpret_cast<float2 *>(base + c.off_part);
+    float *dw_dev = reinterpret_cast<float *>(base + c.off_dw);
+    const int P = c.full.ctas;
+    const size_t row_bytes = (size_t)H * 2;
+    cudaError_t e = cudaSuccess;
+    auto ok = [&](cudaError_t r) {
+        if (e == cudaSuccess)
+            e = r;
+        return e == cudaSuccess;
+    };
+    // everything after the caller's earlier work on `stream`
+    ok(cudaEventRecord(hs->start, s));
+    ok(cudaStreamWaitEvent(hs->in, hs->start, 0));
+    ok(cudaStreamWaitEvent(hs->out, hs->start, 0));
+    ok(cudaMemcpyAsync(base + c.off_w, w, (size_t)H * wb, cudaMemcpyHostToDevice, hs->in));
+    // the last chunk may have fewer CTAs: its missing partials are zeros
+    if (c.last.ctas < P)
+        ok(cudaMemsetAsync(part + ((size_t)(c.chunks - 1) * P + c.last.ctas) * H, 0,
+                           (size_t)(P - c.last.ctas) * H * 8, s));
+    for (int k = 0; k < c.chunks && e == cudaSuccess; ++k) {
+        const int slot = k % c.slots;
+        const uint32_t n = k == c.chunks - 1 ? c.rows_last : c.rows_c;
+        const size_t r0 = (size_t)k * c.rows_c;
+        uint8_t *sb = base + (size_t)slot * c.slot_bytes;
+        if (k >= c.slots)
+            ok(cudaStreamWaitEvent(hs->in, hs->computed[slot], 0)); // inputs of chunk k - slots consumed
+        ok(cudaMemcpyAsync(sb + c.off_x, static_cast<const uint8_t *>(x) + r0 * row_bytes, n * row_bytes,
+                           cudaMemcpyHostToDevice, hs->in));
+        ok(cudaMemcpyAsync(sb + c.off_dy, static_cast<const uint8_t *>(dy) + r0 * row_bytes, n * row_bytes,
+                           cudaMemcpyHostToDevice, hs->in));
+        if (has_dh)
+            ok(cudaMemcpyAsync(sb + c.off_dh, static_cast<const uint8_t *>(dh) + r0 * row_bytes, n * row_bytes,
+                               cudaMemcpyHostToDevice, hs->in));
+        ok(cudaMemcpyAsync(sb + c.off_rstd, rstd + r0, (size_t)n * 4, cudaMemcpyHostToDevice, hs->in));
+        ok(cudaEventRecord(hs->in_ready[slot], hs->in));
+        ok(cudaStreamWaitEvent(s, hs->in_ready[slot], 0));
+        if (k >= c.slots)
+            ok(cudaStreamWaitEvent(s, hs->out_done[slot], 0)); // dx of chunk k - slots copied out
+        ok(launch_chunk_main(k == c.chunks - 1 ? c.last : c.full, H, n, has_dh,
+                             reinterpret_cast<const uint16_t *>(sb + c.off_x),
+                             reinterpret_cast<const uint16_t *>(sb + c.off_dy),
+                             reinterpret_cast<const uint16_t *>(sb + c.off_dh),
+                             reinterpret_cast<const float *>(sb + c.off_rstd), base + c.off_w, w_dtype == CAKE_FP32,
+                             reinterpret_cast<uint16_t *>(sb + c.off_dx), dw_dev, part + (size_t)k * P * H, s));
+        ok(cudaEventRecord(hs->computed[slot], s));
+        ok(cudaStreamWaitEvent(hs->out, hs->computed[slot], 0));
+        ok(cudaMemcpyAsync(static_cast<uint8_t *>(dx) + r0 * row_bytes, sb + c.off_dx, n * row_bytes,
+                           cudaMemcpyDeviceToHost, hs->out));
+        ok(cudaEventRecord(hs->out_done[slot], hs->out));
+    }
+    // dw: every chunk's partials in chunk, then CTA, order
+    if (e == cudaSuccess) {
+        ReduceParams rp{part, c.chunks * P, H, dw_dev, reduce_slices(H, c.chunks * P)};
+        ok(launch_dw_reduce(rp, s));
+    }
+    ok(cudaMemcpyAsync(dw, dw_dev, (size_t)H * 4, cudaMemcpyDeviceToHost, s));
+    // later work on `stream` comes after the last copies of dx
+    ok(cudaEventRecord(hs->end, hs->out));
+    ok(cudaStreamWaitEvent(s, hs->end, 0));
+    return cuda_status(e);
+}
+
 } // namespace
 
 // ---------------------------------------------------------------------------
@@ -1003,6 +1229,26 @@ cake_status cake_rmsnorm_bwd_timeout_test(const cake_shape *shape, const cake_te
     // the grid barrier waits for CTA count + 1 arrivals: it never completes
     return run_bwd(shape, dy, x, rstd, w, w_dtype, nullptr, dx, dw, workspace, workspace_bytes, 1, kFormGrid, -1,
                    stream, kWhole, (uint64_t)wait_limit_us * 1000u, 1);
+}
+
+size_t cake_rmsnorm_bwd_host_staging_size(const cake_shape *shape, cake_dtype w_dtype, int has_dh, int chunks)
+{
+    uint32_t rows = 0;
+    if (check_shape(shape, &rows) != CAKE_OK || rows == 0)
+        return 0;
+    HostChunking c;
+    if (!host_chunking((int)shape->hidden, rows, has_dh != 0, w_dtype == CAKE_FP32 ? 4 : 2, chunks, &c))
+        return 0;
+    return c.total;
+}
+
+cake_status cake_rmsnorm_bwd_host(const cake_shape *shape, const void *dy, const void *x, const float *rstd,
+                                  const void *w, cake_dtype w_dtype, const void *dh, void *dx, float *dw,
+                                  void *staging, size_t staging_bytes, int chunks, int deterministic,
+                                  cake_stream_t stream)
+{
+    (void)deterministic; // both modes run the pair: dw is reproducible either way
+    return run_bwd_host(shape, dy, x, rstd, w, w_dtype, dh, dx, dw, staging, staging_bytes, chunks, stream);
 }
 
 cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, int has_extra,

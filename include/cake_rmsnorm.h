@@ -236,6 +236,42 @@ cake_status cake_rmsnorm_bwd_forced(const cake_shape *shape, const cake_tensor *
                                     int deterministic, int force_single,
                                     int force_accum, cake_stream_t stream);
 
+/* ---- backward from and to host memory -------------------------------------
+ * For rows that live in host memory (a training step whose activations were
+ * offloaded, or a caller measuring the whole path from the host).  The rows
+ * go to the device in `chunks` row chunks (1 .. 64, fewer if there are fewer
+ * rows); the copy of one chunk in, the main kernel of the one before and the
+ * copy of dx out of the one before that overlap, on `stream` (the kernels)
+ * and two copy streams the library creates on a device at its first such
+ * call and keeps.  One fixed-order reduce over the CTA partials of every
+ * chunk then gives dw, so dw is bitwise reproducible for a given shape and
+ * chunk count in both modes (its bits differ from cake_rmsnorm_bwd's, whose
+ * partition is different); dx is the same bits as cake_rmsnorm_bwd's.
+ *
+ *   dy, x, rstd, dh (NULL: none), dx: HOST pointers to dense rows: [T*nh, H]
+ *     BF16 with row stride H (a per-head view is passed as its T*nh rows),
+ *     rstd [T*nh] FP32.  Page-locked memory lets the copies run
+ *     asynchronously and overlap; pageable memory works but serialises.
+ *   w: HOST pointer, [H] of w_dtype.  dw: HOST pointer, [H] FP32, overwritten.
+ *   staging: DEVICE memory owned by the caller, 256-byte aligned, of at least
+ *     cake_rmsnorm_bwd_host_staging_size() bytes (3 slots of chunk inputs and
+ *     dx, the weight, dw and every chunk's partials), else CAKE_ERR_WORKSPACE.
+ *   stream: must belong to the current device (else CAKE_ERR_INVALID); the
+ *     call's copies and kernels come after earlier work on `stream`, and later
+ *     work on `stream` comes after them: dx and dw are in host memory once
+ *     `stream` has reached that point.  Calls on one device are enqueued one
+ *     at a time; they share the copy streams.
+ *   T = 0: dw is zero-filled on the host at once and CAKE_OK returned.
+ */
+size_t cake_rmsnorm_bwd_host_staging_size(const cake_shape *shape, cake_dtype w_dtype, int has_dh,
+                                          int chunks);
+
+cake_status cake_rmsnorm_bwd_host(const cake_shape *shape, const void *dy, const void *x,
+                                  const float *rstd, const void *w, cake_dtype w_dtype,
+                                  const void *dh, void *dx, float *dw, void *staging,
+                                  size_t staging_bytes, int chunks, int deterministic,
+                                  cake_stream_t stream);
+
 /* ---- backward without caller scratch -------------------------------------
  * No counterpart in the pages: an addition of this library.
  *

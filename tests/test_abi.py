@@ -394,3 +394,27 @@ def test_header_is_plain_c_and_the_library_links_from_c(cake, tmp_path):
                            "-L", libdir, "-lcake_rmsnorm", "-Wl,-rpath," + libdir, "-o", str(exe)])
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     assert out[0] == "0" and int(out[1]) > 0 and out[2] == "2" and out[3] == "1"
+
+
+def test_host_path_validation(cake):
+    # the backward from host memory: argument errors come back before any
+    # CUDA call; T = 0 zero-fills dw on the host at once
+    import numpy as np
+    lib = cake.load_library()
+    S = _S(100, 1, 2048)
+    A = 0x100000
+    need = cake.cake_rmsnorm_bwd_host_staging_size((100, 1, 2048), has_dh=False, chunks=4)
+    assert need > 0
+    assert cake.cake_rmsnorm_bwd_host_staging_size((100, 1, 2048), chunks=0) == 0
+    assert cake.cake_rmsnorm_bwd_host_staging_size((100, 1, 2048), chunks=65) == 0
+    call = lambda shape, chunks, staging, nbytes, dw=A: lib.cake_rmsnorm_bwd_host(
+        ctypes.byref(shape), A, A, A, A, 0, None, A, dw, staging, nbytes, chunks, 1, None)
+    assert call(S, 0, A, need) == 1            # chunks out of range
+    assert call(S, 65, A, need) == 1
+    assert call(S, 4, None, need) == 3         # no staging
+    assert call(S, 4, A, need - 1) == 3        # staging too small
+    assert call(S, 4, A + 16, need) == 2       # staging not 256-byte aligned
+    assert call(_S(100, 1, 12), 4, A, need) == 2  # H not a multiple of 8
+    dw = np.full(2048, 5.0, dtype=np.float32)
+    assert call(_S(0, 1, 2048), 4, None, 0, dw=dw.ctypes.data) == 0
+    assert not dw.any()
