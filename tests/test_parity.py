@@ -1,7 +1,7 @@
 """GPU parity: the CUDA path (through the C ABI) against the FP64 oracle,
 element by element, on seeded synthetic inputs.
 
-Bars (the benchmark spec's tolerances, restated in tests/tolerances.py):
+Bars (restated in tests/tolerances.py):
   y     within one BF16 step of RNE_bf16(y64);
   rstd  relative error <= 1e-6 against rstd64;
   h_new bitwise equal to the oracle's RNE_bf16(x + residual);
