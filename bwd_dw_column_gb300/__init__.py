@@ -63,7 +63,8 @@ class _Variant(ctypes.Structure):
     _fields_ = [("single", ctypes.c_int), ("dw_accum", ctypes.c_int), ("vec_per_thread", ctypes.c_int),
                 ("warps_per_row", ctypes.c_int), ("row_groups", ctypes.c_int), ("rows_per_group", ctypes.c_int),
                 ("stages", ctypes.c_int),
-                ("ctas", ctypes.c_int), ("rows_per_cta", ctypes.c_int64), ("smem_bytes", ctypes.c_size_t)]
+                ("ctas", ctypes.c_int), ("rows_per_cta", ctypes.c_int64), ("smem_bytes", ctypes.c_size_t),
+                ("lanes_per_row", ctypes.c_int)]
 
 
 _P = ctypes.POINTER

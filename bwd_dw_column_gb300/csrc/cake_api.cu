@@ -62,7 +62,7 @@ enum Kind { kFwd = 0, kBwd = 1 };
 
 // Developer override of the table, for tuning sweeps: CAKE_TUNE holds
 // comma-separated key=value pairs among vpt, groups, cps, stages, rpg, form,
-// cluster, onecta (backward) and fvpt, fgroups, fcps, fstages (forward).
+// cluster, onecta, half (backward) and fvpt, fgroups, fcps, fstages (forward).
 // Unset, the table below rules.
 // A different row layout (vpt) changes the reduction order and therefore the
 // bits of dx / y / rstd; a different cps or groups changes the pair's
@@ -71,6 +71,7 @@ struct Tune {
     int v[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages, rpg, form+1]
     int cluster = 0;                                         // cluster form: CTAs per cluster
     int one_cta_elems = 0;                                   // backward: one CTA up to rows * H elements
+    int half = -1;                                           // backward rows of half a warp: 0 off, 1 on
 };
 
 static Tune parse_tune(const char *t)
@@ -95,6 +96,8 @@ static Tune parse_tune(const char *t)
             r.cluster = val;
         if (klen == 6 && strncmp(p, "onecta", 6) == 0 && val >= 0)
             r.one_cta_elems = val;
+        if (klen == 4 && strncmp(p, "half", 4) == 0 && (val == 0 || val == 1))
+            r.half = val;
         const char *comma = strchr(eq, ',');
         if (!comma)
             break;
@@ -111,6 +114,7 @@ static const Tune &tune()
 
 struct RowLayout {
     int vpt, W;
+    int half; // rows of 16 lanes, two per warp (vpt 2, W 1)
 };
 
 static RowLayout layout_for(int H, int vpt)
@@ -138,8 +142,26 @@ static RowLayout row_layout(int H, Kind kind)
             return l;
     }
     const int nvec = H / 8;
+    // backward rows of 136 to 256 columns: half a warp per row at 16 columns
+    // per thread, two rows per warp, so that one 4-step butterfly reduces
+    // two rows and each thread's per-row work serves 16 columns instead of 8
+    const int half = tune().half;
+    if (kind == kBwd && nvec > 16 && nvec <= 32 && half != 0)
+        return {2, 1, 1};
+    if (kind == kBwd && nvec <= 32 && half == 1)
+        return {2, 1, 1};
     if (nvec <= 32)
         return {1, 1};
+    // backward rows of 264 to 1024 columns: one warp per row at the fewest
+    // vectors per thread that cover it.  It has as many vector slots as 8
+    // columns per thread on that many warps, but no cross-warp barrier per
+    // row, and 16 to 32 columns share each thread's per-row work (GB300,
+    // deterministic pair, against 8 columns per thread on 2-4 warps: T =
+    // 65536, H = 320 39.2 vs 41.7 us, 384 39.6 vs 42.2, 512 40.8 vs 43.3,
+    // 576 49.4 vs 55.9, 640 49.9 vs 56.5, 704 50.9 vs 57.4, 832 63.7 vs
+    // 69.6; T = 131072, H = 640 88.3 vs 99.2, 832 113.8 vs 127.1)
+    if (kind == kBwd && nvec <= 128)
+        return {(nvec + 31) / 32, 1};
     // backward, 24 or 32 columns per thread where the row splits into W warps
     // with W dividing 12 and enough of the lanes' vectors in use: an SM then
     // holds 12 consumer warps as 12 / W row groups (or, W = 1, as three CTAs
@@ -226,6 +248,8 @@ static int kernel_regs(Kind kind, int vpt, int rpg, int dwm)
         return fwd[vpt];
     if (vpt == 1 && rpg == 2)
         return 96;
+    if (vpt == 2 && rpg == 2)
+        return dwm == CAKE_DW_PLAIN || dwm == CAKE_DW_KAHAN ? 112 : 128; // rows of half a warp
     if (vpt == 1)
         return dwm == CAKE_DW_PLAIN ? 64 : 72;
     return 128;
@@ -250,7 +274,7 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int nten
                       int &ctas_per_sm)
 {
     const int W = rl.W;
-    const int max_warps = (rpg == 2 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
+    const int max_warps = (rpg == 2 && rl.vpt == 1 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
     if (kind == kBwd && W > 1)
         groups = max_warps / W > 1 ? max_warps / W : 1;
     else if (kind == kBwd && rl.vpt > 1)
@@ -298,6 +322,8 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int nten
 // Otherwise one, and more groups per CTA instead.
 static int rows_per_group(const RowLayout &rl, Kind kind)
 {
+    if (rl.half)
+        return 2; // a warp's two half-warp rows
     int rpg = 1;
     const int one_row_groups = (kMaxThreadsFor(rl.vpt) / 32 - 1) / rl.W;
     if (kind == kBwd && rl.W > 1 && one_row_groups < 2)
@@ -321,8 +347,17 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     p.lo_bytes = lo_smem(kind, dwm, p.rl, p.groups);
     const size_t fixed = (size_t)kMiscBytes + weight_smem_bytes(H) + p.lo_bytes;
     int stages = per_cta > fixed ? (int)((per_cta - fixed) / stage) : 0;
-    if (tune().v[kind][3] >= 2 && tune().v[kind][3] < stages)
-        stages = tune().v[kind][3];
+    // backward rows of one warp or half a warp at 16 or more columns per
+    // thread: at most four stages, fewer bytes in flight than would fit
+    // (GB300: [T, 24, 256] strided per-head views at T = 32768 192 us
+    // against 199-206 us with 3, 5, 6 or 8 stages; [T, 4, 256] 33.3 us
+    // against 34.3-35.0 us; H = 512, T = 131072 71.9 us against 73.6 us
+    // with 7 stages)
+    int want = kind == kBwd && p.rl.W == 1 && p.rl.vpt >= 2 ? 4 : kMaxStages;
+    if (tune().v[kind][3] >= 2)
+        want = tune().v[kind][3];
+    if (want < stages)
+        stages = want;
     if (stages > kMaxStages)
         stages = kMaxStages;
     if (stages < 2) { // fewer CTAs per SM so that at least two stages fit
@@ -602,6 +637,7 @@ void fill_variant(const Plan &p, cake_variant *out)
     out->ctas = p.ctas;
     out->rows_per_cta = p.rows_per_cta;
     out->smem_bytes = p.smem;
+    out->lanes_per_row = p.rl.half ? 16 : 32;
 }
 
 cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, int force_single,
@@ -623,8 +659,9 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
     if (force_accum >= 0)
         dwm = force_accum;
     *plan = make_plan((int)shape->hidden, *rows, has_dh ? 3 : 2, kBwd, single, dwm);
+    // the tree form is built for 8 or 16 columns per thread
     if (plan->single == kFormTree &&
-        (plan->rl.vpt != 1 || plan->rpg != 1 || tree_groups(plan->ctas) > kTreeMaxGroups))
+        (plan->rl.vpt > 2 || (plan->rl.vpt == 1 && plan->rpg != 1) || tree_groups(plan->ctas) > kTreeMaxGroups))
         return CAKE_ERR_UNSUPPORTED;
     return CAKE_OK;
 }

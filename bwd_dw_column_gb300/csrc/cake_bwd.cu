@@ -89,13 +89,17 @@ __global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __gr
 
 // ------------------------------------------------------------------ launch
 
-// Row build of a plan: 1 two rows per group, 4 rows of one warp at 8
-// columns per thread, 0 otherwise.
-static int row_build(const Layout &L, int vpt)
+// The row build of a layout: 5 rows of half a warp (two 8-column vectors
+// per thread, two rows per warp and group), 1 two rows per group of one
+// vector per thread, 4 rows of one warp at 8 columns per thread, 0
+// otherwise; -1 for a combination no build serves.
+static int row_build(int vpt, int W, int rpg, int threads)
 {
-    if (L.rows_per_group == 2)
-        return 1;
-    return vpt == 1 && L.warps_per_row == 1 ? 4 : 0;
+    if (rpg == 2 && vpt == 2)
+        return W == 1 && threads <= kMaxThreadsFor(2) ? 5 : -1;
+    if (rpg == 2)
+        return vpt == 1 && threads <= kMaxThreadsR2 ? 1 : -1;
+    return vpt == 1 && W == 1 ? 4 : 0;
 }
 
 cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, int ctas, size_t smem,
@@ -107,8 +111,9 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
         if (e != cudaSuccess)
             return e;
     }
-    const int rb = row_build(q.L, vpt);
-    if (rb == 1 && (vpt != 1 || 32 * (q.L.groups * q.L.warps_per_row + 1) > kMaxThreadsR2))
+    const int rb = row_build(vpt, q.L.warps_per_row, q.L.rows_per_group,
+                             32 * (q.L.groups * q.L.warps_per_row + 1));
+    if (rb < 0)
         return cudaErrorInvalidValue;
     switch (single) {
     case kFormPair: return launch_bwd_form<kFormPair>(q, vpt, rb, dwm, ctas, smem, stream);
@@ -142,8 +147,8 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
 
 cudaError_t occupancy_bwd(int vpt, int w, int rpg, int single, int dwm, int threads, size_t smem, int *n)
 {
-    const int rb = rpg == 2 ? 1 : (vpt == 1 && w == 1 ? 4 : 0);
-    if (rb == 1 && (vpt != 1 || threads > kMaxThreadsR2))
+    const int rb = row_build(vpt, w, rpg, threads);
+    if (rb < 0)
         return cudaErrorInvalidValue;
     switch (single) {
     case kFormPair: return occ_bwd_form<kFormPair>(vpt, rb, dwm, threads, smem, n);

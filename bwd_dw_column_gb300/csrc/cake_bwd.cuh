@@ -44,7 +44,7 @@
 
 namespace cake {
 
-template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1>
+template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1, bool HALF = false>
 __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -83,20 +83,32 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     const int gtid = wig * 32 + lane;
     const int nvec = L.nvec;
     const bool has_dh = L.ntens == 3;
+    // HALF: rows of 16 lanes, two per warp -- lanes 0-15 hold the group's
+    // first row of a tile and lanes 16-31 its second, so one 4-step butterfly
+    // reduces both; a thread's vectors are k * 16 + (lane & 15).  Otherwise
+    // a row spans the group's W warps and a thread's vectors are
+    // k * 32 * W + gtid.
+    const int sub = HALF ? (lane >> 4) : 0;
+    const int ltid = HALF ? (lane & 15) : gtid;
+    const int vstride = HALF ? 16 : 32 * W;
+    const bool owner = !HALF || sub == 0; // holds the combined partial at the end
+    constexpr int RG = HALF ? 2 : R2;     // rows a group owns per tile
 
     // (with 8 columns per thread the element-wise staging measured 3-6 %
     // faster over a whole T = 65536 step, although it costs up to 3 us more
     // at small T)
     stage_weight<VPT != 1>(s, L, p.w, p.w_f32);
-    // with 8 columns per thread a thread's columns are the same on every row:
-    // keep their weights in registers instead of reading shared memory per
-    // row (GB300: 3 % off the main kernel for rows of 256 and 640 with plain
-    // or blocked sums; the Kahan and TwoSum builds would spill, so they keep
-    // reading shared memory)
-    constexpr bool kWreg = VPT == 1 && (DWM == CAKE_DWM_PLAIN || DWM == CAKE_DWM_BLOCKED);
-    float2 wreg[4];
+    // with 8 columns per thread (or 16 on rows of half a warp) a thread's
+    // columns are the same on every row: keep their weights in registers
+    // instead of reading shared memory per row (GB300: 3 % off the main
+    // kernel for rows of 256 and 640 with plain or blocked sums; the Kahan
+    // and TwoSum builds would spill, so they keep reading shared memory)
+    constexpr bool kWreg = (VPT == 1 || HALF) && (DWM == CAKE_DWM_PLAIN || DWM == CAKE_DWM_BLOCKED);
+    float2 wreg[kWreg ? VPT : 1][4];
     if constexpr (kWreg)
-        weight_pairs(s, L, gtid < nvec ? gtid : 0, wreg);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            weight_pairs(s, L, k * vstride + ltid < nvec ? k * vstride + ltid : 0, wreg[k]);
 
     // dw accumulators for this thread's columns (pairs of adjacent columns):
     // the partial is hi + lo in every form.
@@ -168,7 +180,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 
     // A group owns R2 consecutive rows of every tile: gid*R2 + i.
     auto rs_of = [&](uint32_t tile, int i) {
-        const uint32_t r = c.r0 + tile * c.tile_rows + gid * R2 + i;
+        const uint32_t r = c.r0 + tile * c.tile_rows + gid * RG + sub + i;
         return (tile < c.ntiles && r < c.r_end) ? __ldg(p.rstd + r) : 0.f;
     };
     // rstd of this group's rows, loaded kAhead tiles ahead (a register ring)
@@ -190,16 +202,17 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             rsn[i] = rs_of(it + kAhead, i);
         abort = !mbar_wait(smem_addr(&s.full[st]), ph, p.wait_ns);
         const uint8_t *stage = s.ring + st * s.stage_bytes;
-        const uint32_t rbase = c.r0 + it * c.tile_rows + gid * R2;
-        const int nrow = rbase < c.r_end ? (int)min((uint32_t)R2, c.r_end - rbase) : 0; // uniform in the group
-        if (nrow > 0) {
+        const uint32_t gbase = c.r0 + it * c.tile_rows + gid * RG; // the group's first row
+        const uint32_t rbase = gbase + sub;                           // this thread's first row
+        const int nrow = rbase < c.r_end ? (int)min((uint32_t)R2, c.r_end - rbase) : 0; // uniform in the group but for HALF
+        if (gbase < c.r_end) {
             // One pass over each staged row: m = dy*w and the row dot sum m*h
             // (even / odd columns in the two lanes, in the order of k and q;
             // then lane 0 + lane 1; then the group reduction), and the dw
             // terms dy*h*rstd (dy*h is exact in FP32), rows in order.
             // VPT == 1 keeps x and m in registers for the dx step; wider
             // layouts re-read the staged row instead (fewer registers).
-            constexpr bool kKeep = VPT == 1 && KEEP;
+            constexpr bool kKeep = (VPT == 1 || HALF) && KEEP;
             float2 x2[R2][kKeep ? VPT : 1][4], m2[R2][kKeep ? VPT : 1][4];
             float dot[R2];
 #pragma unroll
@@ -207,7 +220,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                 dot[i] = 0.f;
                 if (i >= nrow)
                     continue;
-                const int tr = gid * R2 + i;
+                const int tr = gid * RG + sub + i;
                 const float rs = rsr[0][i];
                 const float2 rs2 = make_float2(rs, rs);
                 const float2 nrs2 = make_float2(-rs, -rs);
@@ -216,7 +229,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                 float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    const int v = k * 32 * W + gtid;
+                    const int v = k * vstride + ltid;
                     uint4 xr = make_uint4(0, 0, 0, 0), dr = make_uint4(0, 0, 0, 0);
                     if (v < nvec) {
                         xr = xs[v];
@@ -226,7 +239,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                     if constexpr (kWreg) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            w2[q] = wreg[q];
+                            w2[q] = wreg[k][q];
                     } else {
                         weight_pairs(s, L, v < nvec ? v : 0, w2);
                     }
@@ -270,13 +283,22 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                 dot[i] = __fadd_rn(dot2.x, dot2.y);
             }
             float tot[R2];
-            group_sum_n<R2, W1 ? 1 : 0>(dot, tot, s, L, gid, wig, lane, slot++, abort);
+            if constexpr (HALF) {
+                // both rows of the warp at once: a butterfly within each half
+                tot[0] = dot[0];
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1)
+                    tot[0] += __shfl_xor_sync(0xffffffffu, tot[0], o);
+                abort = __any_sync(0xffffffffu, abort);
+            } else {
+                group_sum_n<R2, W1 ? 1 : 0>(dot, tot, s, L, gid, wig, lane, slot++, abort);
+            }
 
 #pragma unroll
             for (int i = 0; i < R2; ++i) {
                 if (i >= nrow)
                     continue;
-                const int tr = gid * R2 + i;
+                const int tr = gid * RG + sub + i;
                 const float rs = rsr[0][i];
                 const float2 rs2 = make_float2(rs, rs);
                 // dx_j = rs*(g_j - xhat_j*c) = m_j*rs - h_j*kk, kk = ((tot/H)*rs)*rs*rs:
@@ -291,7 +313,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                     p.dx + out_off(p.dx_st, p.dx_sh, p.dx_row_stride, p.dx_uniform, rbase + i, L.nh);
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    const int v = k * 32 * W + gtid;
+                    const int v = k * vstride + ltid;
                     if (v < nvec && !abort) {
                         uint4 hv = make_uint4(0, 0, 0, 0);
                         if (has_dh)
@@ -301,7 +323,13 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                         if (!kKeep) {
                             xr2 = xs[v];
                             dr2 = dys[v];
-                            weight_pairs(s, L, v, w2);
+                            if constexpr (kWreg) {
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    w2[q] = wreg[k][q];
+                            } else {
+                                weight_pairs(s, L, v, w2);
+                            }
                         }
                         uint32_t o[4];
 #pragma unroll
@@ -352,6 +380,23 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             }
         }
     }
+    if constexpr (HALF) {
+        // lanes 16-31 summed the tile's second rows over the same columns as
+        // lanes 0-15: fold their partial into the lower half's
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float hx = __shfl_down_sync(0xffffffffu, hi[k][q].x, 16);
+                const float lx = __shfl_down_sync(0xffffffffu, lo[k][q].x, 16);
+                const float hy = __shfl_down_sync(0xffffffffu, hi[k][q].y, 16);
+                const float ly = __shfl_down_sync(0xffffffffu, lo[k][q].y, 16);
+                comp_add(hi[k][q].x, lo[k][q].x, hx);
+                lo[k][q].x = __fadd_rn(lo[k][q].x, lx);
+                comp_add(hi[k][q].y, lo[k][q].y, hy);
+                lo[k][q].y = __fadd_rn(lo[k][q].y, ly);
+            }
+    }
     if (FORM == kFormPair)
         pdl_launch_dependents();
 
@@ -365,8 +410,8 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         if (gid > 0) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                if (v < nvec)
+                const int v = k * vstride + ltid;
+                if (owner && v < nvec)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         comb[((gid - 1) * 4 + q) * nvec + v] =
@@ -378,8 +423,8 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             for (int g = 1; g < L.groups; ++g) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    const int v = k * 32 * W + gtid;
-                    if (v < nvec)
+                    const int v = k * vstride + ltid;
+                    if (owner && v < nvec)
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float4 a = comb[((g - 1) * 4 + q) * nvec + v];
@@ -404,8 +449,8 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         if (gid == 0) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                if (v < nvec)
+                const int v = k * vstride + ltid;
+                if (owner && v < nvec)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         mine[v * 4 + q] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
@@ -468,8 +513,8 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             if (gid == 0) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    const int v = k * 32 * W + gtid;
-                    if (v < nvec) {
+                    const int v = k * vstride + ltid;
+                    if (owner && v < nvec) {
                         float o[8];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -490,8 +535,8 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                if (v < nvec)
+                const int v = k * vstride + ltid;
+                if (owner && v < nvec)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         dst[v * 4 + q] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
@@ -606,8 +651,8 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         double *acc = p.acc + (size_t)(blockIdx.x % p.banks) * ncol;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int v = k * 32 * W + gtid;
-            if (v < nvec)
+            const int v = k * vstride + ltid;
+            if (owner && v < nvec)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     atomicAdd(acc + v * 8 + 2 * q, (double)hi[k][q].x + (double)lo[k][q].x);
@@ -648,14 +693,15 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 // The row kernels, by row build RB: 0 one row per group; 1 two rows per
 // group (one group of up to 16 warps and the producer per CTA), keeping x and
 // dy*w of both rows in registers; 4 one row per group for rows of one warp
-// (H <= 256), with that width known to the compiler.  The bounds cap the
-// registers a thread may use so that the largest CTA fits: 72 (26 warps),
-// 96 (17 warps), 128 (13 warps).
+// (H <= 256), with that width known to the compiler; 5 (VPT = 2) rows of
+// half a warp, two per warp (H <= 256).  The bounds cap the registers a
+// thread may use so that the largest CTA fits: 72 (26 warps), 96 (17
+// warps), 128 (13 warps).
 template <int VPT, int DWM, int FORM, int RB>
 __global__ void __launch_bounds__(RB == 1 ? kMaxThreadsR2 : kMaxThreadsFor(VPT), 1)
     bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
-    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4>(p);
+    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4 || RB == 5, RB == 5>(p);
 }
 
 // ------------------------------------------------------------------ launch
@@ -740,13 +786,16 @@ static cudaError_t occ_dwm(int dwm, int threads, size_t smem, int *n)
 }
 
 // One form's launcher and occupancy query over the row builds it is compiled
-// for: (VPT, RB) = (1, 0), (1, 1), (1, 4), (2, 0), (3, 0), (4, 0); the tree
-// form only (1, 0), which also serves rows of one warp.
+// for: (VPT, RB) = (1, 0), (1, 1), (1, 4), (2, 0), (2, 5), (3, 0), (4, 0);
+// the tree form only (1, 0), which also serves rows of one warp, (2, 0) and
+// (2, 5).
 template <int FORM>
 cudaError_t launch_bwd_form(const BwdParams &p, int vpt, int rb, int dwm, int ctas, size_t smem,
                             cudaStream_t stream)
 {
+    if (vpt == 2 && rb == 5) return launch_dwm<2, FORM, 5>(p, dwm, ctas, smem, stream);
     if constexpr (FORM == kFormTree) {
+        if (vpt == 2 && rb == 0) return launch_dwm<2, FORM, 0>(p, dwm, ctas, smem, stream);
         return vpt == 1 && rb != 1 ? launch_dwm<1, FORM, 0>(p, dwm, ctas, smem, stream) : cudaErrorInvalidValue;
     } else {
         if (vpt == 1 && rb == 1) return launch_dwm<1, FORM, 1>(p, dwm, ctas, smem, stream);
@@ -765,7 +814,9 @@ cudaError_t launch_bwd_form(const BwdParams &p, int vpt, int rb, int dwm, int ct
 template <int FORM>
 cudaError_t occ_bwd_form(int vpt, int rb, int dwm, int threads, size_t smem, int *n)
 {
+    if (vpt == 2 && rb == 5) return occ_dwm<2, FORM, 5>(dwm, threads, smem, n);
     if constexpr (FORM == kFormTree) {
+        if (vpt == 2 && rb == 0) return occ_dwm<2, FORM, 0>(dwm, threads, smem, n);
         return vpt == 1 && rb != 1 ? occ_dwm<1, FORM, 0>(dwm, threads, smem, n) : cudaErrorInvalidValue;
     } else {
         if (vpt == 1 && rb == 1) return occ_dwm<1, FORM, 1>(dwm, threads, smem, n);

@@ -204,13 +204,15 @@ typedef struct {
                           CTA order (deterministic; no workspace) */
     int dw_accum;      /* cake_dw_accum */
     int vec_per_thread; /* 16-byte vectors of a row held by each thread */
-    int warps_per_row; /* warps that share one row */
+    int warps_per_row; /* warps that share one row (1 where lanes_per_row is 16) */
     int row_groups;    /* row groups (of warps_per_row warps) per CTA */
     int rows_per_group; /* rows each group owns per pipeline stage (1 or 2) */
     int stages;        /* depth of the shared-memory ring */
     int ctas;          /* CTAs launched (P, also the number of dw partials) */
     int64_t rows_per_cta; /* contiguous rows each CTA owns */
     size_t smem_bytes; /* dynamic shared memory per CTA */
+    int lanes_per_row; /* 32 x warps_per_row lanes, or 16: rows of half a
+                          warp, two per warp (rows_per_group 2) */
 } cake_variant;
 
 /*
@@ -219,9 +221,9 @@ typedef struct {
  * cake_variant.single) / force_accum (-1 = let the table decide) override
  * the table, as the tests that sweep every variant do; deterministic = 1
  * refuses force_single = 1 with CAKE_ERR_INVALID; force_single = 2 needs a
- * row layout of 8 columns per thread with one row per group (the table's
- * choice for H <= 512 and a few widths between 1032 and 1144), else
- * CAKE_ERR_UNSUPPORTED.
+ * row layout of 8 columns per thread with one row per group or of 16
+ * columns per thread (the table's choice for H <= 512 and for 1032 to
+ * 1336), else CAKE_ERR_UNSUPPORTED.
  */
 cake_status cake_rmsnorm_bwd_select(const cake_shape *shape, cake_dtype w_dtype,
                                     int deterministic, int has_dh, int force_single,

@@ -98,14 +98,26 @@ def test_every_width_plans_a_valid_launch(cake):
 
 
 def test_row_layout_depends_on_h_alone(cake):
-    for H in (256, 1536, 2048, 6144):
+    for H in (200, 256, 1536, 2048, 6144):
         layouts = set()
         for T in (1, 5, 300, 70000):
             for det in (True, False):
                 for dh in (False, True):
                     v = cake.cake_rmsnorm_bwd_select((T, 1, H), deterministic=det, has_dh=dh)
-                    layouts.add((v["vec_per_thread"], v["warps_per_row"]))
+                    layouts.add((v["vec_per_thread"], v["warps_per_row"], v["lanes_per_row"]))
         assert len(layouts) == 1, (H, layouts)
+
+
+@pytest.mark.parametrize("H,half", [(8, False), (128, False), (136, True), (200, True), (256, True), (264, False),
+                                    (512, False)])
+def test_half_warp_rows(cake, H, half):
+    # backward rows of 136 to 256 columns: 16 lanes of 16 columns per row, two
+    # rows per warp and per group; other widths keep whole warps
+    v = cake.cake_rmsnorm_bwd_select((4096, 1, H), deterministic=True)
+    if half:
+        assert (v["lanes_per_row"], v["vec_per_thread"], v["warps_per_row"], v["rows_per_group"]) == (16, 2, 1, 2), v
+    else:
+        assert v["lanes_per_row"] == 32 and not (v["vec_per_thread"] == 2 and v["rows_per_group"] == 2), v
 
 
 @pytest.mark.parametrize("shape,one", [((1, 1, 1536), True), ((16, 1, 1536), True), ((17, 1, 1536), False),
@@ -319,7 +331,7 @@ def test_row_groups_fit_named_barriers(cake):
 def test_row_group_override_is_capped(cake, tune):
     # the tuning override cannot push a multi-warp row past the barrier ids
     code = ("import bwd_dw_column_gb300 as c, json; "
-            "print(json.dumps([c.cake_rmsnorm_bwd_select((65536, 1, H)) for H in (512, 1536, 2048, 1040)]))")
+            "print(json.dumps([c.cake_rmsnorm_bwd_select((65536, 1, H)) for H in (1152, 1536, 2048, 1040)]))")
     env = dict(os.environ, CAKE_TUNE=tune)
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT, check=True)
     for v in json.loads(out.stdout.strip().splitlines()[-1]):
@@ -350,8 +362,12 @@ def _bwd_forced(cake, shape, dy, x, rstd, w, dh, dx, dw, ws, nbytes, det, single
 
 
 def test_tree_form_selection(cake):
+    # rows of 256 run at half a warp per row in every form, the tree included,
+    # so that dx has the same bits whichever form is picked
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), deterministic=True, force_single=2)
-    assert v["single"] == 2 and v["vec_per_thread"] == 1
+    assert v["single"] == 2 and v["vec_per_thread"] == 2 and v["lanes_per_row"] == 16
+    v = cake.cake_rmsnorm_bwd_select((32768, 4, 128), deterministic=True, force_single=2)
+    assert v["single"] == 2 and v["vec_per_thread"] == 1 and v["lanes_per_row"] == 32
     v = cake.cake_rmsnorm_bwd_select((1000, 1, 512), deterministic=False, force_single=2)
     assert v["single"] == 2
     for H in (2048, 8192):  # 32 and 24 columns per thread: no tree form

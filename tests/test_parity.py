@@ -263,8 +263,14 @@ def check_bwd(cake, x, dy, w, eps, residual=None, dh=None, variants=VARIANTS, dw
     return worst
 
 
-BWD_SHAPES = [(1, 8), (2, 16), (3, 24), (37, 256), (5, 520), (300, 1536), (129, 2048), (33, 4096), (17, 5120),
-              (40, 6144), (9, 8192), (1000, 2048)]
+# rows of 136 to 256 run at half a warp per row, two rows per warp: 2 x 136
+# and 333 x 200 leave part of each thread's second vector idle, 1001 x 256
+# spans several CTAs and ends on a tile whose second half-warp has no row;
+# rows of 384 to 1024 run on one warp at 16 to 32 columns per thread (61 x
+# 384 as one CTA, 700 x 512, 1003 x 640, 257 x 832 over several)
+BWD_SHAPES = [(1, 8), (2, 16), (3, 24), (2, 136), (37, 256), (333, 200), (1001, 256), (61, 384), (700, 512),
+              (1003, 640), (257, 832), (5, 520), (300, 1536), (129, 2048), (33, 4096), (17, 5120), (40, 6144),
+              (9, 8192), (1000, 2048)]
 
 
 @pytest.mark.parametrize("T,H", BWD_SHAPES)
@@ -275,7 +281,7 @@ def test_bwd_plain(cake, T, H, w_dtype):
 
 
 @pytest.mark.parametrize("family", ["outlier", "offset", "rowmean"])
-@pytest.mark.parametrize("T,H", [(700, 2048), (2500, 1536)])
+@pytest.mark.parametrize("T,H", [(700, 2048), (2500, 1536), (2501, 256)])
 def test_bwd_families(cake, family, T, H):
     # the input families of the accuracy sweep, through every form; 2500 rows
     # take the blocked dw sums
