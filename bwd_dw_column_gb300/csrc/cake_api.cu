@@ -62,7 +62,8 @@ enum Kind { kFwd = 0, kBwd = 1 };
 
 // Developer override of the table, for tuning sweeps: CAKE_TUNE holds
 // comma-separated key=value pairs among vpt, groups, cps, stages, rpg, form,
-// cluster, onecta, half (backward) and fvpt, fgroups, fcps, fstages (forward).
+// cluster, onecta, half, rslices (backward) and fvpt, fgroups, fcps, fstages
+// (forward).
 // Unset, the table below rules.
 // A different row layout (vpt) changes the reduction order and therefore the
 // bits of dx / y / rstd; a different cps or groups changes the pair's
@@ -72,6 +73,7 @@ struct Tune {
     int cluster = 0;                                         // cluster form: CTAs per cluster
     int one_cta_elems = 0;                                   // backward: one CTA up to rows * H elements
     int half = -1;                                           // backward rows of half a warp: 0 off, 1 on
+    int rslices = 0;                                         // the pair's reduce: partial ranges per column and warp
 };
 
 static Tune parse_tune(const char *t)
@@ -98,6 +100,8 @@ static Tune parse_tune(const char *t)
             r.one_cta_elems = val;
         if (klen == 4 && strncmp(p, "half", 4) == 0 && (val == 0 || val == 1))
             r.half = val;
+        if (klen == 7 && strncmp(p, "rslices", 7) == 0 && (val == 1 || val == 2 || val == 4 || val == 8))
+            r.rslices = val;
         const char *comma = strchr(eq, ',');
         if (!comma)
             break;
@@ -446,13 +450,20 @@ static void pick_variant(uint32_t rows, int deterministic, int &single, int &dwm
         dwm = CAKE_DW_TWOSUM;
 }
 
-// Partial ranges per column per warp of the fixed-order reduce: about one
-// CTA per SM or more where H allows, and at most 8 partials per lane (one
-// round of loads in flight).
+// Partial ranges per column per warp of the fixed-order reduce: doubled
+// while the grid stays within one CTA per SM, or while a lane would sum more
+// than 32 partials.  Fewer, longer-running CTAs beat a grid of several per
+// SM, even with three rounds of loads per lane (GB300, the pair's reduce
+// after its main kernel: H = 5120, 304 partials, 3.9 us with 160 CTAs
+// against 5.5 us with 640; H = 4096 and 6144 at 152 partials 3.0 and 3.4 us
+// with 128 and 192 CTAs against 5.2 and 5.8 us with 512 and 768; H = 2048
+// 2.1 us at 128 CTAs, 3.1 us at 64 and 256).
 static int reduce_slices(int H, int P)
 {
+    if (tune().rslices > 0)
+        return tune().rslices;
     int S = 1;
-    while (S < 8 && ((H + 32 / S - 1) / (32 / S) < kSMs || (P + 16 * S - 1) / (16 * S) > 8))
+    while (S < 8 && ((H + 16 / S - 1) / (16 / S) <= kSMs || (P + 16 * S - 1) / (16 * S) > 32))
         S *= 2;
     return S;
 }
