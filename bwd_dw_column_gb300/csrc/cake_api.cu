@@ -372,8 +372,8 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     }
     p.stages = stages;
     p.smem = ring_smem(ntens, p.groups * p.rpg, H, stages, p.lo_bytes);
-    // the group-combine buffer reuses the ring
-    const size_t comb = fixed + (size_t)(p.groups > 1 ? p.groups - 1 : 0) * H * 8;
+    // the backward's group-combine buffer (every group's partial) reuses the ring
+    const size_t comb = fixed + (size_t)(kind == kBwd ? p.groups : 0) * H * 8;
     if (comb > p.smem)
         p.smem = comb;
     const uint32_t tile = (uint32_t)(p.groups * p.rpg);
@@ -401,8 +401,8 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
             C = (int)by_tiles;
         p.rows_per_cta = (rows + C - 1) / C;
         p.ctas = (int)((rows + p.rows_per_cta - 1) / p.rows_per_cta);
-        // its partial lives in the drained ring
-        const size_t part = fixed + (size_t)H * 8;
+        // its partial lives in the drained ring, past the group-combine buffer
+        const size_t part = fixed + (size_t)(p.groups + 1) * H * 8;
         if (part > p.smem)
             p.smem = part;
     }

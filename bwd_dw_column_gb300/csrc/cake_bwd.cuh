@@ -44,6 +44,40 @@
 
 namespace cake {
 
+// Slot m = 4 v + q of the CTA partial (columns 8 v + 2 q and the next one,
+// float4 (hi.x, lo.x, hi.y, lo.y)) summed over the row groups' partials in
+// shared memory ([group][q][vector]) in group order.
+__device__ __forceinline__ float4 slot_sum(const float4 *comb, int nvec, int groups, int m)
+{
+    const int v = m >> 2, q = m & 3;
+    float4 a = comb[q * nvec + v];
+#pragma unroll 1
+    for (int g = 1; g < groups; ++g) {
+        const float4 b = comb[(g * 4 + q) * nvec + v];
+        comp_add(a.x, a.y, b.x);
+        a.y = __fadd_rn(a.y, b.y);
+        comp_add(a.z, a.w, b.z);
+        a.w = __fadd_rn(a.w, b.w);
+    }
+    return a;
+}
+
+// The pair's CTA partial to global memory (or, for a pair of one CTA, dw
+// itself: hi + lo rounded once, the bits the reduce of one partial gives).
+// Not inlined, so that none of its addressing is hoisted into the row loop,
+// whose widest builds use every register a thread may have.
+static __device__ __noinline__ void emit_pair_partial(const float4 *comb, int nvec, int groups, int nthr, float4 *dst,
+                                               float2 *dw, int direct)
+{
+    for (int m = (int)threadIdx.x; m < 4 * nvec; m += nthr) {
+        const float4 a = slot_sum(comb, nvec, groups, m);
+        if (direct)
+            dw[m] = make_float2(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w));
+        else
+            dst[m] = a;
+    }
+}
+
 template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1, bool HALF = false>
 __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 {
@@ -93,6 +127,22 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     const int vstride = HALF ? 16 : 32 * W;
     const bool owner = !HALF || sub == 0; // holds the combined partial at the end
     constexpr int RG = HALF ? 2 : R2;     // rows a group owns per tile
+
+    // This thread's rows of tile `tile`: gid*RG + sub + i, i < R2.
+    auto rs_of = [&](uint32_t tile, int i) {
+        const uint32_t r = c.r0 + tile * c.tile_rows + gid * RG + sub + i;
+        return (tile < c.ntiles && r < c.r_end) ? __ldg(p.rstd + r) : 0.f;
+    };
+    // rstd of this group's rows, loaded kAhead tiles ahead (a register ring);
+    // the first loads go out before the weight is staged, so that their
+    // latency overlaps the weight's
+    constexpr int kAhead = R2 == 1 ? 4 : 2;
+    float rsr[kAhead][R2];
+#pragma unroll
+    for (int d = 0; d < kAhead; ++d)
+#pragma unroll
+        for (int i = 0; i < R2; ++i)
+            rsr[d][i] = rs_of(d, i);
 
     // (with 8 columns per thread the element-wise staging measured 3-6 %
     // faster over a whole T = 65536 step, although it costs up to 3 us more
@@ -178,19 +228,6 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             plane(k) = make_float4(0.f, 0.f, 0.f, 0.f);
     int blk_rows = 0;
 
-    // A group owns R2 consecutive rows of every tile: gid*R2 + i.
-    auto rs_of = [&](uint32_t tile, int i) {
-        const uint32_t r = c.r0 + tile * c.tile_rows + gid * RG + sub + i;
-        return (tile < c.ntiles && r < c.r_end) ? __ldg(p.rstd + r) : 0.f;
-    };
-    // rstd of this group's rows, loaded kAhead tiles ahead (a register ring)
-    constexpr int kAhead = R2 == 1 ? 4 : 2;
-    float rsr[kAhead][R2];
-#pragma unroll
-    for (int d = 0; d < kAhead; ++d)
-#pragma unroll
-        for (int i = 0; i < R2; ++i)
-            rsr[d][i] = rs_of(d, i);
 
     bool abort = false;
     uint32_t slot = 0;
@@ -397,65 +434,41 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                 lo[k][q].y = __fadd_rn(lo[k][q].y, ly);
             }
     }
-    if (FORM == kFormPair)
-        pdl_launch_dependents();
 
-    // ---- combine the row groups' partials in group order (shared memory,
-    // [group - 1][q][vector] float4 (hi.x, lo.x, hi.y, lo.y): a warp's lanes
-    // touch consecutive 16-byte slots, free of bank conflicts)
+    // ---- the CTA partial.  Every row group writes its partial to shared
+    // memory ([group][q][vector] float4 (hi.x, lo.x, hi.y, lo.y): a warp's
+    // lanes touch consecutive 16-byte slots, free of bank conflicts), then
+    // every consumer thread sums whole slots over the groups in group order
+    // -- slot m = 4 v + q holds columns 8 v + 2 q and the next one -- so the
+    // combine is spread over the CTA instead of left to one group.
     consumer_sync(L);
     float4 *comb = reinterpret_cast<float4 *>(s.ring);
     const int ncol = nvec * 8;
-    if (L.groups > 1) {
-        if (gid > 0) {
+    const int nslot = 4 * nvec;
+    const int nthr = consumer_warps * 32;
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * vstride + ltid;
-                if (owner && v < nvec)
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * vstride + ltid;
+        if (owner && v < nvec)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        comb[((gid - 1) * 4 + q) * nvec + v] =
-                            make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
-            }
-        }
-        consumer_sync(L);
-        if (gid == 0) {
-            for (int g = 1; g < L.groups; ++g) {
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int v = k * vstride + ltid;
-                    if (owner && v < nvec)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 a = comb[((g - 1) * 4 + q) * nvec + v];
-                            comp_add(hi[k][q].x, lo[k][q].x, a.x);
-                            lo[k][q].x = __fadd_rn(lo[k][q].x, a.y);
-                            comp_add(hi[k][q].y, lo[k][q].y, a.z);
-                            lo[k][q].y = __fadd_rn(lo[k][q].y, a.w);
-                        }
-                }
-            }
-        }
+            for (int q = 0; q < 4; ++q)
+                comb[(gid * 4 + q) * nvec + v] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
     }
+    consumer_sync(L);
+    // calls emit(m, slot) for each of this thread's slots of the CTA partial
+    auto for_each_slot = [&](auto &&emit) {
+        for (int m = (int)threadIdx.x; m < nslot; m += nthr)
+            emit(m, slot_sum(comb, nvec, L.groups, m));
+    };
 
     if constexpr (FORM == kFormCluster) {
         // ---- cluster form: the CTA's partial goes to its own shared memory
-        // (the drained ring, once group 0 has read the combine buffer), as
-        // float2 (hi, lo) per column; thread 0 then tells every CTA of the
-        // cluster, and each CTA, once all have told it, reduces its slice of
-        // the columns over the cluster's partials in CTA order.
-        consumer_sync(L);
-        float4 *mine = reinterpret_cast<float4 *>(s.ring);
-        if (gid == 0) {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * vstride + ltid;
-                if (owner && v < nvec)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        mine[v * 4 + q] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
-            }
-        }
+        // (the drained ring, past the combine buffer), as float2 (hi, lo) per
+        // column; thread 0 then tells every CTA of the cluster, and each CTA,
+        // once all have told it, reduces its slice of the columns over the
+        // cluster's partials in CTA order.
+        float4 *mine = comb + L.groups * nslot;
+        for_each_slot([&](int m, float4 a) { mine[m] = a; });
         consumer_sync(L);
         const uint32_t C = (uint32_t)p.cluster;
         if (threadIdx.x == 0) {
@@ -480,18 +493,21 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         const int j0 = (int)rank * per, j1 = min(ncol, j0 + per);
         const uint32_t base = smem_addr(mine);
         for (int j = j0 + (int)threadIdx.x; j < j1; j += consumer_warps * 32) {
-            float2 v[kMaxCluster];
-#pragma unroll
-            for (int r = 0; r < kMaxCluster; ++r)
-                v[r] = r < (int)C ? ld_cluster_f2(map_to_rank(base + 8u * (uint32_t)j, (uint32_t)r))
-                                  : make_float2(0.f, 0.f);
+            // CTA order, four remote loads in flight at a time
             float h = 0.f, l = 0.f;
+            for (int r0 = 0; r0 < (int)C; r0 += 4) {
+                float2 v[4];
 #pragma unroll
-            for (int r = 0; r < kMaxCluster; ++r)
-                if (r < (int)C) {
-                    comp_add(h, l, v[r].x);
-                    l = __fadd_rn(l, v[r].y);
-                }
+                for (int u = 0; u < 4; ++u)
+                    v[u] = r0 + u < (int)C ? ld_cluster_f2(map_to_rank(base + 8u * (uint32_t)j, (uint32_t)(r0 + u)))
+                                           : make_float2(0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (r0 + u < (int)C) {
+                        comp_add(h, l, v[u].x);
+                        l = __fadd_rn(l, v[u].y);
+                    }
+            }
             p.dw[j] = __fadd_rn(h, l);
         }
         // this CTA's remote reads are complete: tell every CTA, and keep this
@@ -507,43 +523,18 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     }
 
     if constexpr (FORM == kFormPair) {
-        if (p.direct_dw) {
-            // a pair of one CTA: its partial is dw (the reduce of a single
-            // partial would give the same bits, hi + lo rounded once)
-            if (gid == 0) {
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int v = k * vstride + ltid;
-                    if (owner && v < nvec) {
-                        float o[8];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            o[2 * q] = __fadd_rn(hi[k][q].x, lo[k][q].x);
-                            o[2 * q + 1] = __fadd_rn(hi[k][q].y, lo[k][q].y);
-                        }
-                        float4 *d4 = reinterpret_cast<float4 *>(p.dw) + 2 * v;
-                        d4[0] = make_float4(o[0], o[1], o[2], o[3]);
-                        d4[1] = make_float4(o[4], o[5], o[6], o[7]);
-                    }
-                }
-            }
-            return;
-        }
+        // the CTA partial, or for a pair of one CTA dw itself (the reduce of
+        // a single partial would give the same bits, hi + lo rounded once)
+        emit_pair_partial(comb, nvec, L.groups, nthr, reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol),
+                          reinterpret_cast<float2 *>(p.dw), p.direct_dw);
+        // the reduce may launch once every CTA has written its partial (GB300:
+        // 1-2 us faster at T = 4096 than a trigger before the group combine)
+        pdl_launch_dependents();
+        return;
     }
     if (FORM != kFormAtomic) {
-        if (gid == 0) {
-            float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * vstride + ltid;
-                if (owner && v < nvec)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[v * 4 + q] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
-            }
-        }
-        if (FORM == kFormPair)
-            return;
+        float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);
+        for_each_slot([&](int m, float4 a) { dst[m] = a; });
         if (FORM == kFormGrid) {
             // ---- cooperative form: every CTA's partial is written; after
             // the grid barrier CTA b reduces columns [b*C, (b+1)*C), one
@@ -647,18 +638,12 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     // ---- single kernel: FP64 column accumulation into one of `banks` copies
     // of the accumulators (CTA b adds into bank b % banks, which spreads the
     // L2 atomics); the last CTA to arrive sums the banks and finalises
-    if (gid == 0) {
+    {
         double *acc = p.acc + (size_t)(blockIdx.x % p.banks) * ncol;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * vstride + ltid;
-            if (owner && v < nvec)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    atomicAdd(acc + v * 8 + 2 * q, (double)hi[k][q].x + (double)lo[k][q].x);
-                    atomicAdd(acc + v * 8 + 2 * q + 1, (double)hi[k][q].y + (double)lo[k][q].y);
-                }
-        }
+        for_each_slot([&](int m, float4 a) {
+            atomicAdd(acc + 2 * m, (double)a.x + (double)a.y);
+            atomicAdd(acc + 2 * m + 1, (double)a.z + (double)a.w);
+        });
         __threadfence();
     }
     consumer_sync(L);
