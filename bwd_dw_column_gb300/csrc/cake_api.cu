@@ -274,8 +274,8 @@ static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int warps_per_ct
 // 7 % faster as 3 groups, and the fewer CTA partials shorten the dw
 // reduction).  Otherwise about 8 consumer warps per CTA, then as many CTAs
 // per SM as the register file holds (at most 3).
-static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int ntens, int &groups,
-                      int &ctas_per_sm)
+static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int ntens, uint32_t rows, bool one_cta,
+                      int &groups, int &ctas_per_sm)
 {
     const int W = rl.W;
     const int max_warps = (rpg == 2 && rl.vpt == 1 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
@@ -287,6 +287,14 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int nten
         groups = max_warps / W > 1 ? max_warps / W : 1; // plain forward: see the cap below
     else
         groups = W >= 8 ? 1 : 8 / W;
+    // backward rows of several warps, at most two per SM and more than one
+    // CTA's worth: two row groups per CTA, so that more CTAs (and SMs) share
+    // the rows (GB300, ncu spans of the pair at T = 64 and 256: H = 1536 9.4
+    // and 9.8 us against 10.1 and 10.6 us with six groups; H = 4096 10.7 and
+    // 12.1 us against 11.5 and 12.4 us with three; from T = 1024, and for
+    // rows of one warp, fewer groups cost time)
+    if (kind == kBwd && W > 1 && groups > 2 && !one_cta && rows <= (uint32_t)(kSMs * 2 * rpg))
+        groups = 2;
     const Tune &t = tune();
     if (t.v[kind][1] > 0)
         groups = t.v[kind][1];
@@ -345,7 +353,9 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     Plan p;
     p.rl = row_layout(H, kind);
     p.rpg = rows_per_group(p.rl, kind);
-    cta_shape(p.rl, kind, p.rpg, dwm, ntens, p.groups, p.ctas_per_sm);
+    const int64_t one_cta = tune().one_cta_elems > 0 ? tune().one_cta_elems : kOneCtaElems;
+    const bool one_cta_rows = kind == kBwd && (int64_t)rows * H <= one_cta;
+    cta_shape(p.rl, kind, p.rpg, dwm, ntens, rows, one_cta_rows, p.groups, p.ctas_per_sm);
     const size_t per_cta = kSmemPerSM / p.ctas_per_sm;
     const size_t stage = (size_t)ntens * p.groups * p.rpg * H * 2;
     p.lo_bytes = lo_smem(kind, dwm, p.rl, p.groups);
@@ -386,8 +396,7 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     // 10.2 us for two CTAs and the reduce; H = 4096 T = 4 10.5 against 12.3;
     // H = 6144 T = 4 11.8 against 13.1; even at H = 1536 T = 16 and H = 256
     // T = 64, slower beyond: one SM cannot stream more rows in time)
-    const int64_t one_cta = tune().one_cta_elems > 0 ? tune().one_cta_elems : kOneCtaElems;
-    if (kind == kBwd && ctas > 1 && (int64_t)rows * H <= one_cta)
+    if (one_cta_rows && ctas > 1)
         ctas = 1;
     p.rows_per_cta = ctas ? (rows + ctas - 1) / ctas : 0;
     p.ctas = p.rows_per_cta ? (int)((rows + p.rows_per_cta - 1) / p.rows_per_cta) : 0;
