@@ -131,6 +131,17 @@ def test_small_row_sets_run_as_one_cta(cake, shape, one):
         assert (v["ctas"] == 1) == one, (shape, v)
 
 
+@pytest.mark.parametrize("shape,groups", [((64, 1, 1536), 2), ((304, 1, 1536), 2), ((305, 1, 1536), 6),
+                                          ((16, 1, 1536), 6), ((256, 1, 4096), 2), ((1024, 1, 4096), 3),
+                                          ((256, 1, 256), 4), ((256, 1, 6144), 2)])
+def test_few_rows_of_several_warps_take_two_groups(cake, shape, groups):
+    # up to two rows per SM, rows of several warps run as CTAs of two row
+    # groups (more CTAs share the rows); one-CTA row sets and rows of one warp
+    # keep their groups
+    v = cake.cake_rmsnorm_bwd_select(shape, deterministic=True)
+    assert v["row_groups"] == groups, (shape, v)
+
+
 def test_partition_depends_on_shape_alone(cake):
     a = cake.cake_rmsnorm_bwd_select((65536, 1, 2048), deterministic=True)
     b = cake.cake_rmsnorm_bwd_select((65536, 1, 2048), deterministic=True)
