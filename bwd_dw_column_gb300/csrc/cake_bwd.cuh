@@ -46,18 +46,27 @@ namespace cake {
 
 // Slot m = 4 v + q of the CTA partial (columns 8 v + 2 q and the next one,
 // float4 (hi.x, lo.x, hi.y, lo.y)) summed over the row groups' partials in
-// shared memory ([group][q][vector]) in group order.
-__device__ __forceinline__ float4 slot_sum(const float4 *comb, int nvec, int groups, int m)
+// shared memory (at shared address comb, [group][q][vector]) in group order,
+// four groups' loads in flight at a time.
+__device__ __forceinline__ float4 slot_sum(uint32_t comb, int nvec, int groups, int m)
 {
     const int v = m >> 2, q = m & 3;
-    float4 a = comb[q * nvec + v];
-#pragma unroll 1
-    for (int g = 1; g < groups; ++g) {
-        const float4 b = comb[(g * 4 + q) * nvec + v];
-        comp_add(a.x, a.y, b.x);
-        a.y = __fadd_rn(a.y, b.y);
-        comp_add(a.z, a.w, b.z);
-        a.w = __fadd_rn(a.w, b.w);
+    const uint32_t base = comb + 16u * (uint32_t)(q * nvec + v);
+    const uint32_t gstride = 64u * (uint32_t)nvec;
+    float4 a = ld_shared_f4(base);
+    for (int g0 = 1; g0 < groups; g0 += 4) {
+        float4 b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            b[u] = g0 + u < groups ? ld_shared_f4(base + (uint32_t)(g0 + u) * gstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (g0 + u < groups) {
+                comp_add(a.x, a.y, b[u].x);
+                a.y = __fadd_rn(a.y, b[u].y);
+                comp_add(a.z, a.w, b[u].z);
+                a.w = __fadd_rn(a.w, b[u].w);
+            }
     }
     return a;
 }
@@ -66,8 +75,8 @@ __device__ __forceinline__ float4 slot_sum(const float4 *comb, int nvec, int gro
 // itself: hi + lo rounded once, the bits the reduce of one partial gives).
 // Not inlined, so that none of its addressing is hoisted into the row loop,
 // whose widest builds use every register a thread may have.
-static __device__ __noinline__ void emit_pair_partial(const float4 *comb, int nvec, int groups, int nthr, float4 *dst,
-                                               float2 *dw, int direct)
+static __device__ __noinline__ void emit_pair_partial(uint32_t comb, int nvec, int groups, int nthr, float4 *dst,
+                                                      float2 *dw, int direct)
 {
     for (int m = (int)threadIdx.x; m < 4 * nvec; m += nthr) {
         const float4 a = slot_sum(comb, nvec, groups, m);
@@ -458,7 +467,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     // calls emit(m, slot) for each of this thread's slots of the CTA partial
     auto for_each_slot = [&](auto &&emit) {
         for (int m = (int)threadIdx.x; m < nslot; m += nthr)
-            emit(m, slot_sum(comb, nvec, L.groups, m));
+            emit(m, slot_sum(smem_addr(comb), nvec, L.groups, m));
     };
 
     if constexpr (FORM == kFormCluster) {
@@ -525,7 +534,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     if constexpr (FORM == kFormPair) {
         // the CTA partial, or for a pair of one CTA dw itself (the reduce of
         // a single partial would give the same bits, hi + lo rounded once)
-        emit_pair_partial(comb, nvec, L.groups, nthr, reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol),
+        emit_pair_partial(smem_addr(comb), nvec, L.groups, nthr, reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol),
                           reinterpret_cast<float2 *>(p.dw), p.direct_dw);
         // the reduce may launch once every CTA has written its partial (GB300:
         // 1-2 us faster at T = 4096 than a trigger before the group combine)

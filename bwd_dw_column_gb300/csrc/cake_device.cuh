@@ -154,6 +154,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
 }
 
+// Load a float4 from this CTA's shared memory.  Volatile, so that a batch of
+// them is issued in program order after the barrier before it, and in flight
+// together until their values are used.
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 // Load a float2 from another CTA's shared memory (distributed shared memory).
 __device__ __forceinline__ float2 ld_cluster_f2(uint32_t cluster_addr)
 {
