@@ -72,7 +72,7 @@ struct Tune {
     int v[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages, rpg, form+1]
     int cluster = 0;                                         // cluster form: CTAs per cluster
     int one_cta_elems = 0;                                   // backward: one CTA up to rows * H elements
-    int half = -1;                                           // backward rows of half a warp: 0 off, 1 on
+    int half = -1;                                           // backward rows of part of a warp: 0 off
     int rslices = 0;                                         // the pair's reduce: partial ranges per column and warp
 };
 
@@ -118,7 +118,7 @@ static const Tune &tune()
 
 struct RowLayout {
     int vpt, W;
-    int half; // rows of 16 lanes, two per warp (vpt 2, W 1)
+    int lanes; // rows of part of a warp: lanes per row (16 or 8; W 1); 0: whole warps
 };
 
 static RowLayout layout_for(int H, int vpt)
@@ -146,14 +146,16 @@ static RowLayout row_layout(int H, Kind kind)
             return l;
     }
     const int nvec = H / 8;
-    // backward rows of 136 to 256 columns: half a warp per row at 16 columns
-    // per thread, two rows per warp, so that one 4-step butterfly reduces
-    // two rows and each thread's per-row work serves 16 columns instead of 8
-    const int half = tune().half;
-    if (kind == kBwd && nvec > 16 && nvec <= 32 && half != 0)
-        return {2, 1, 1};
-    if (kind == kBwd && nvec <= 32 && half == 1)
-        return {2, 1, 1};
+    // backward rows of at most 256 columns: part of a warp per row, so that
+    // one short butterfly reduces several rows and no lane idles -- 136 to
+    // 256 columns on half a warp at 16 columns per thread, 72 to 128 on half
+    // a warp at 8, at most 64 on a quarter of a warp at 8 (two or four rows
+    // per warp)
+    if (kind == kBwd && nvec <= 32 && tune().half != 0) {
+        if (nvec > 16)
+            return {2, 1, 16};
+        return {1, 1, nvec > 8 ? 16 : 8};
+    }
     if (nvec <= 32)
         return {1, 1};
     // backward rows of 264 to 1024 columns: one warp per row at the fewest
@@ -245,23 +247,25 @@ static size_t lo_smem(Kind kind, int dwm, const RowLayout &rl, int groups)
 // Registers per thread of each row kernel as compiled for sm_103a (ptxas
 // -v), by kind and VPT; the resident-CTA count below follows from them and
 // a GPU test checks it against the occupancy the runtime reports.
-static int kernel_regs(Kind kind, int vpt, int rpg, int dwm)
+static int kernel_regs(Kind kind, int vpt, int rpg, int dwm, int lanes)
 {
     static const int fwd[5] = {0, 48, 64, 80, 96};
     if (kind == kFwd)
         return fwd[vpt];
+    if (lanes && vpt == 2)
+        return dwm == CAKE_DW_PLAIN || dwm == CAKE_DW_KAHAN ? 112 : 128; // rows of half a warp
+    if (lanes)
+        return 72; // rows of a half or a quarter of a warp at 8 columns per thread
     if (vpt == 1 && rpg == 2)
         return 96;
-    if (vpt == 2 && rpg == 2)
-        return dwm == CAKE_DW_PLAIN || dwm == CAKE_DW_KAHAN ? 112 : 128; // rows of half a warp
     if (vpt == 1)
         return dwm == CAKE_DW_PLAIN ? 64 : 72;
     return 128;
 }
 
-static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int warps_per_cta)
+static int resident_limit(Kind kind, int vpt, int rpg, int dwm, int lanes, int warps_per_cta)
 {
-    const int regs = (kernel_regs(kind, vpt, rpg, dwm) + 7) & ~7;
+    const int regs = (kernel_regs(kind, vpt, rpg, dwm, lanes) + 7) & ~7;
     const int by_regs = 65536 / (warps_per_cta * 32 * regs);
     const int by_warps = 64 / warps_per_cta;
     return by_regs < by_warps ? by_regs : by_warps;
@@ -278,7 +282,7 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int nten
                       int &groups, int &ctas_per_sm)
 {
     const int W = rl.W;
-    const int max_warps = (rpg == 2 && rl.vpt == 1 ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
+    const int max_warps = (rpg == 2 && rl.vpt == 1 && !rl.lanes ? kMaxThreadsR2 : kMaxThreadsFor(rl.vpt)) / 32 - 1; // consumer warps per CTA
     if (kind == kBwd && W > 1)
         groups = max_warps / W > 1 ? max_warps / W : 1;
     else if (kind == kBwd && rl.vpt > 1)
@@ -302,7 +306,7 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int nten
         --groups;
     if (W > 1 && groups > kMaxRowGroupBarriers) // one named barrier per group
         groups = kMaxRowGroupBarriers;
-    ctas_per_sm = resident_limit(kind, rl.vpt, rpg, dwm, groups * W + 1);
+    ctas_per_sm = resident_limit(kind, rl.vpt, rpg, dwm, rl.lanes, groups * W + 1);
     // at most 3 resident CTAs; the forward's warp-per-row layout takes 4,
     // and its 4-warps-per-row layout runs best at 2 (GB300 measurements)
     int cap = 3;
@@ -334,8 +338,8 @@ static void cta_shape(const RowLayout &rl, Kind kind, int rpg, int dwm, int nten
 // Otherwise one, and more groups per CTA instead.
 static int rows_per_group(const RowLayout &rl, Kind kind)
 {
-    if (rl.half)
-        return 2; // a warp's two half-warp rows
+    if (rl.lanes)
+        return 32 / rl.lanes; // a warp's rows of part of a warp
     int rpg = 1;
     const int one_row_groups = (kMaxThreadsFor(rl.vpt) / 32 - 1) / rl.W;
     if (kind == kBwd && rl.W > 1 && one_row_groups < 2)
@@ -367,7 +371,7 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     // against 199-206 us with 3, 5, 6 or 8 stages; [T, 4, 256] 33.3 us
     // against 34.3-35.0 us; H = 512, T = 131072 71.9 us against 73.6 us
     // with 7 stages)
-    int want = kind == kBwd && p.rl.W == 1 && p.rl.vpt >= 2 ? 4 : kMaxStages;
+    int want = kind == kBwd && p.rl.W == 1 && (p.rl.vpt >= 2 || p.rl.lanes) ? 4 : kMaxStages;
     if (tune().v[kind][3] >= 2)
         want = tune().v[kind][3];
     if (want < stages)
@@ -635,6 +639,7 @@ Layout make_layout(const Plan &p, int H, uint32_t rows, uint32_t nh, int ntens)
     L.warps_per_row = p.rl.W;
     L.groups = p.groups;
     L.rows_per_group = p.rpg;
+    L.lanes_per_row = p.rl.lanes ? p.rl.lanes : 32;
     L.stages = p.stages;
     L.lo_bytes = (int)p.lo_bytes;
     L.ntens = ntens;
@@ -657,7 +662,7 @@ void fill_variant(const Plan &p, cake_variant *out)
     out->ctas = p.ctas;
     out->rows_per_cta = p.rows_per_cta;
     out->smem_bytes = p.smem;
-    out->lanes_per_row = p.rl.half ? 16 : 32;
+    out->lanes_per_row = p.rl.lanes ? p.rl.lanes : 32;
 }
 
 cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, int force_single,
@@ -681,7 +686,8 @@ cake_status select_plan(const cake_shape *shape, int deterministic, int has_dh, 
     *plan = make_plan((int)shape->hidden, *rows, has_dh ? 3 : 2, kBwd, single, dwm);
     // the tree form is built for 8 or 16 columns per thread
     if (plan->single == kFormTree &&
-        (plan->rl.vpt > 2 || (plan->rl.vpt == 1 && plan->rpg != 1) || tree_groups(plan->ctas) > kTreeMaxGroups))
+        (plan->rl.vpt > 2 || (plan->rl.vpt == 1 && plan->rpg != 1 && !plan->rl.lanes) ||
+         tree_groups(plan->ctas) > kTreeMaxGroups))
         return CAKE_ERR_UNSUPPORTED;
     return CAKE_OK;
 }
@@ -1328,7 +1334,7 @@ cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, i
         return st;
     const int threads = 32 * (plan.groups * plan.rl.W + 1);
     int n = 0;
-    cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.rl.W, plan.rpg, plan.single, plan.dwm, threads, plan.smem, &n)
+    cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.rl.W, plan.rpg, plan.rl.lanes ? plan.rl.lanes : 32, plan.single, plan.dwm, threads, plan.smem, &n)
                              : occupancy_fwd(plan.rl.vpt, threads, plan.smem, &n);
     if (e != cudaSuccess)
         return CAKE_ERR_CUDA;

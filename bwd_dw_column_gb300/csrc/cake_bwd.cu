@@ -89,14 +89,22 @@ __global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __gr
 
 // ------------------------------------------------------------------ launch
 
-// The row build of a layout: 5 rows of half a warp (two 8-column vectors
-// per thread, two rows per warp and group), 1 two rows per group of one
-// vector per thread, 4 rows of one warp at 8 columns per thread, 0
-// otherwise; -1 for a combination no build serves.
-static int row_build(int vpt, int W, int rpg, int threads)
+// The row build of a layout: rows of part of a warp -- 5 half a warp at
+// two 8-column vectors per thread, 6 half a warp at one, 7 a quarter at one
+// (one warp per group, 32 / lanes rows per warp and group); 1 two rows per
+// group of one vector per thread; 4 rows of one warp at 8 columns per
+// thread; 0 otherwise; -1 for a combination no build serves.
+static int row_build(int vpt, int W, int rpg, int lanes, int threads)
 {
-    if (rpg == 2 && vpt == 2)
-        return W == 1 && threads <= kMaxThreadsFor(2) ? 5 : -1;
+    if (lanes == 16 || lanes == 8) {
+        if (W != 1 || rpg != 32 / lanes || threads > kMaxThreadsFor(vpt))
+            return -1;
+        if (lanes == 16)
+            return vpt == 2 ? 5 : vpt == 1 ? 6 : -1;
+        return vpt == 1 ? 7 : -1;
+    }
+    if (lanes != 32)
+        return -1;
     if (rpg == 2)
         return vpt == 1 && threads <= kMaxThreadsR2 ? 1 : -1;
     return vpt == 1 && W == 1 ? 4 : 0;
@@ -111,7 +119,7 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
         if (e != cudaSuccess)
             return e;
     }
-    const int rb = row_build(vpt, q.L.warps_per_row, q.L.rows_per_group,
+    const int rb = row_build(vpt, q.L.warps_per_row, q.L.rows_per_group, q.L.lanes_per_row,
                              32 * (q.L.groups * q.L.warps_per_row + 1));
     if (rb < 0)
         return cudaErrorInvalidValue;
@@ -145,9 +153,9 @@ cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-cudaError_t occupancy_bwd(int vpt, int w, int rpg, int single, int dwm, int threads, size_t smem, int *n)
+cudaError_t occupancy_bwd(int vpt, int w, int rpg, int lanes, int single, int dwm, int threads, size_t smem, int *n)
 {
-    const int rb = row_build(vpt, w, rpg, threads);
+    const int rb = row_build(vpt, w, rpg, lanes, threads);
     if (rb < 0)
         return cudaErrorInvalidValue;
     switch (single) {

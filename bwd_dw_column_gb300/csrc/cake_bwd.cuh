@@ -87,7 +87,7 @@ static __device__ __noinline__ void emit_pair_partial(uint32_t comb, int nvec, i
     }
 }
 
-template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1, bool HALF = false>
+template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1, int LPR = 32>
 __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -126,16 +126,17 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     const int gtid = wig * 32 + lane;
     const int nvec = L.nvec;
     const bool has_dh = L.ntens == 3;
-    // HALF: rows of 16 lanes, two per warp -- lanes 0-15 hold the group's
-    // first row of a tile and lanes 16-31 its second, so one 4-step butterfly
-    // reduces both; a thread's vectors are k * 16 + (lane & 15).  Otherwise
-    // a row spans the group's W warps and a thread's vectors are
-    // k * 32 * W + gtid.
-    const int sub = HALF ? (lane >> 4) : 0;
-    const int ltid = HALF ? (lane & 15) : gtid;
-    const int vstride = HALF ? 16 : 32 * W;
-    const bool owner = !HALF || sub == 0; // holds the combined partial at the end
-    constexpr int RG = HALF ? 2 : R2;     // rows a group owns per tile
+    // LPR < 32: rows of LPR lanes (16 or 8), 32 / LPR per warp -- lanes
+    // [s * LPR, (s + 1) * LPR) hold the group's row s of a tile, so one
+    // log2(LPR)-step butterfly reduces them all; a thread's vectors are
+    // k * LPR + lane % LPR.  Otherwise a row spans the group's W warps and a
+    // thread's vectors are k * 32 * W + gtid.
+    constexpr bool SUB = LPR < 32;
+    const int sub = SUB ? lane / LPR : 0;
+    const int ltid = SUB ? lane % LPR : gtid;
+    const int vstride = SUB ? LPR : 32 * W;
+    const bool owner = !SUB || sub == 0; // holds the combined partial at the end
+    constexpr int RG = SUB ? 32 / LPR : R2; // rows a group owns per tile
 
     // This thread's rows of tile `tile`: gid*RG + sub + i, i < R2.
     auto rs_of = [&](uint32_t tile, int i) {
@@ -162,7 +163,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     // instead of reading shared memory per row (GB300: 3 % off the main
     // kernel for rows of 256 and 640 with plain or blocked sums; the Kahan
     // and TwoSum builds would spill, so they keep reading shared memory)
-    constexpr bool kWreg = (VPT == 1 || HALF) && (DWM == CAKE_DWM_PLAIN || DWM == CAKE_DWM_BLOCKED);
+    constexpr bool kWreg = (VPT == 1 || SUB) && (DWM == CAKE_DWM_PLAIN || DWM == CAKE_DWM_BLOCKED);
     float2 wreg[kWreg ? VPT : 1][4];
     if constexpr (kWreg)
 #pragma unroll
@@ -250,7 +251,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         const uint8_t *stage = s.ring + st * s.stage_bytes;
         const uint32_t gbase = c.r0 + it * c.tile_rows + gid * RG; // the group's first row
         const uint32_t rbase = gbase + sub;                           // this thread's first row
-        const int nrow = rbase < c.r_end ? (int)min((uint32_t)R2, c.r_end - rbase) : 0; // uniform in the group but for HALF
+        const int nrow = rbase < c.r_end ? (int)min((uint32_t)R2, c.r_end - rbase) : 0; // uniform in the group but for SUB
         if (gbase < c.r_end) {
             // One pass over each staged row: m = dy*w and the row dot sum m*h
             // (even / odd columns in the two lanes, in the order of k and q;
@@ -258,7 +259,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             // terms dy*h*rstd (dy*h is exact in FP32), rows in order.
             // VPT == 1 keeps x and m in registers for the dx step; wider
             // layouts re-read the staged row instead (fewer registers).
-            constexpr bool kKeep = (VPT == 1 || HALF) && KEEP;
+            constexpr bool kKeep = (VPT == 1 || SUB) && KEEP;
             float2 x2[R2][kKeep ? VPT : 1][4], m2[R2][kKeep ? VPT : 1][4];
             float dot[R2];
 #pragma unroll
@@ -329,11 +330,11 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
                 dot[i] = __fadd_rn(dot2.x, dot2.y);
             }
             float tot[R2];
-            if constexpr (HALF) {
-                // both rows of the warp at once: a butterfly within each half
+            if constexpr (SUB) {
+                // every row of the warp at once: a butterfly within each row's lanes
                 tot[0] = dot[0];
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1)
+                for (int o = LPR / 2; o > 0; o >>= 1)
                     tot[0] += __shfl_xor_sync(0xffffffffu, tot[0], o);
                 abort = __any_sync(0xffffffffu, abort);
             } else {
@@ -426,22 +427,25 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
             }
         }
     }
-    if constexpr (HALF) {
-        // lanes 16-31 summed the tile's second rows over the same columns as
-        // lanes 0-15: fold their partial into the lower half's
+    if constexpr (SUB) {
+        // the lanes of rows 1 .. 32 / LPR - 1 summed the tile's other rows
+        // over the same columns as row 0's lanes: fold their partials into
+        // row 0's, in a fixed order (pairs 16 apart, then 8 apart)
 #pragma unroll
-        for (int k = 0; k < VPT; ++k)
+        for (int d = 16; d >= LPR; d >>= 1)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float hx = __shfl_down_sync(0xffffffffu, hi[k][q].x, 16);
-                const float lx = __shfl_down_sync(0xffffffffu, lo[k][q].x, 16);
-                const float hy = __shfl_down_sync(0xffffffffu, hi[k][q].y, 16);
-                const float ly = __shfl_down_sync(0xffffffffu, lo[k][q].y, 16);
-                comp_add(hi[k][q].x, lo[k][q].x, hx);
-                lo[k][q].x = __fadd_rn(lo[k][q].x, lx);
-                comp_add(hi[k][q].y, lo[k][q].y, hy);
-                lo[k][q].y = __fadd_rn(lo[k][q].y, ly);
-            }
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float hx = __shfl_down_sync(0xffffffffu, hi[k][q].x, d);
+                    const float lx = __shfl_down_sync(0xffffffffu, lo[k][q].x, d);
+                    const float hy = __shfl_down_sync(0xffffffffu, hi[k][q].y, d);
+                    const float ly = __shfl_down_sync(0xffffffffu, lo[k][q].y, d);
+                    comp_add(hi[k][q].x, lo[k][q].x, hx);
+                    lo[k][q].x = __fadd_rn(lo[k][q].x, lx);
+                    comp_add(hi[k][q].y, lo[k][q].y, hy);
+                    lo[k][q].y = __fadd_rn(lo[k][q].y, ly);
+                }
     }
 
     // ---- the CTA partial.  Every row group writes its partial to shared
@@ -687,15 +691,15 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 // The row kernels, by row build RB: 0 one row per group; 1 two rows per
 // group (one group of up to 16 warps and the producer per CTA), keeping x and
 // dy*w of both rows in registers; 4 one row per group for rows of one warp
-// (H <= 256), with that width known to the compiler; 5 (VPT = 2) rows of
-// half a warp, two per warp (H <= 256).  The bounds cap the registers a
-// thread may use so that the largest CTA fits: 72 (26 warps), 96 (17
-// warps), 128 (13 warps).
+// (H <= 256), with that width known to the compiler; rows of part of a warp:
+// 5 (VPT = 2) and 6 (VPT = 1) half a warp, two rows per warp; 7 (VPT = 1) a
+// quarter, four rows per warp.  The bounds cap the registers a thread may use
+// so that the largest CTA fits: 72 (26 warps), 96 (17 warps), 128 (13 warps).
 template <int VPT, int DWM, int FORM, int RB>
 __global__ void __launch_bounds__(RB == 1 ? kMaxThreadsR2 : kMaxThreadsFor(VPT), 1)
     bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
-    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4 || RB == 5, RB == 5>(p);
+    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4 || RB >= 5, RB == 5 || RB == 6 ? 16 : RB == 7 ? 8 : 32>(p);
 }
 
 // ------------------------------------------------------------------ launch
@@ -780,14 +784,16 @@ static cudaError_t occ_dwm(int dwm, int threads, size_t smem, int *n)
 }
 
 // One form's launcher and occupancy query over the row builds it is compiled
-// for: (VPT, RB) = (1, 0), (1, 1), (1, 4), (2, 0), (2, 5), (3, 0), (4, 0);
-// the tree form only (1, 0), which also serves rows of one warp, (2, 0) and
-// (2, 5).
+// for: (VPT, RB) = (1, 0), (1, 1), (1, 4), (1, 6), (1, 7), (2, 0), (2, 5),
+// (3, 0), (4, 0); the tree form only (1, 0), which also serves rows of one
+// warp, (1, 6), (1, 7), (2, 0) and (2, 5).
 template <int FORM>
 cudaError_t launch_bwd_form(const BwdParams &p, int vpt, int rb, int dwm, int ctas, size_t smem,
                             cudaStream_t stream)
 {
     if (vpt == 2 && rb == 5) return launch_dwm<2, FORM, 5>(p, dwm, ctas, smem, stream);
+    if (vpt == 1 && rb == 6) return launch_dwm<1, FORM, 6>(p, dwm, ctas, smem, stream);
+    if (vpt == 1 && rb == 7) return launch_dwm<1, FORM, 7>(p, dwm, ctas, smem, stream);
     if constexpr (FORM == kFormTree) {
         if (vpt == 2 && rb == 0) return launch_dwm<2, FORM, 0>(p, dwm, ctas, smem, stream);
         return vpt == 1 && rb != 1 ? launch_dwm<1, FORM, 0>(p, dwm, ctas, smem, stream) : cudaErrorInvalidValue;
@@ -809,6 +815,8 @@ template <int FORM>
 cudaError_t occ_bwd_form(int vpt, int rb, int dwm, int threads, size_t smem, int *n)
 {
     if (vpt == 2 && rb == 5) return occ_dwm<2, FORM, 5>(dwm, threads, smem, n);
+    if (vpt == 1 && rb == 6) return occ_dwm<1, FORM, 6>(dwm, threads, smem, n);
+    if (vpt == 1 && rb == 7) return occ_dwm<1, FORM, 7>(dwm, threads, smem, n);
     if constexpr (FORM == kFormTree) {
         if (vpt == 2 && rb == 0) return occ_dwm<2, FORM, 0>(dwm, threads, smem, n);
         return vpt == 1 && rb != 1 ? occ_dwm<1, FORM, 0>(dwm, threads, smem, n) : cudaErrorInvalidValue;

@@ -82,7 +82,8 @@ struct Layout {
     int nvec;           // H / 8: 16-byte vectors per row
     int warps_per_row;  // W
     int groups;         // NG
-    int rows_per_group; // rows a group owns per stage (1, or 2 for the backward)
+    int rows_per_group; // rows a group owns per stage (1; the backward 2, or 32 / lanes_per_row)
+    int lanes_per_row;  // the backward: 32 (rows of whole warps), 16 or 8 (rows of part of a warp)
     int stages;         // ring depth
     int lo_bytes;       // backward, blocked dw sums: the per-thread compensated pairs kept in
                         // shared memory ([2 or 4 * VPT float4][consumer threads]); 0 otherwise

@@ -204,15 +204,16 @@ typedef struct {
                           CTA order (deterministic; no workspace) */
     int dw_accum;      /* cake_dw_accum */
     int vec_per_thread; /* 16-byte vectors of a row held by each thread */
-    int warps_per_row; /* warps that share one row (1 where lanes_per_row is 16) */
+    int warps_per_row; /* warps that share one row (1 where lanes_per_row is 16 or 8) */
     int row_groups;    /* row groups (of warps_per_row warps) per CTA */
-    int rows_per_group; /* rows each group owns per pipeline stage (1 or 2) */
+    int rows_per_group; /* rows each group owns per pipeline stage (1, 2 or 4) */
     int stages;        /* depth of the shared-memory ring */
     int ctas;          /* CTAs launched (P, also the number of dw partials) */
     int64_t rows_per_cta; /* contiguous rows each CTA owns */
     size_t smem_bytes; /* dynamic shared memory per CTA */
-    int lanes_per_row; /* 32 x warps_per_row lanes, or 16: rows of half a
-                          warp, two per warp (rows_per_group 2) */
+    int lanes_per_row; /* 32 x warps_per_row lanes, or 16 or 8: rows of part
+                          of a warp, 32 / lanes_per_row per warp
+                          (= rows_per_group) */
 } cake_variant;
 
 /*

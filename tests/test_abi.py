@@ -108,16 +108,17 @@ def test_row_layout_depends_on_h_alone(cake):
         assert len(layouts) == 1, (H, layouts)
 
 
-@pytest.mark.parametrize("H,half", [(8, False), (128, False), (136, True), (200, True), (256, True), (264, False),
-                                    (512, False)])
-def test_half_warp_rows(cake, H, half):
-    # backward rows of 136 to 256 columns: 16 lanes of 16 columns per row, two
-    # rows per warp and per group; other widths keep whole warps
+@pytest.mark.parametrize("H,layout", [(8, (8, 1, 4)), (64, (8, 1, 4)), (72, (16, 1, 2)), (128, (16, 1, 2)),
+                                      (136, (16, 2, 2)), (200, (16, 2, 2)), (256, (16, 2, 2)), (264, (32, 2, 1)),
+                                      (512, (32, 2, 1))])
+def test_part_warp_rows(cake, H, layout):
+    # backward rows of at most 256 columns take part of a warp: a quarter up
+    # to 64 columns, a half above, at 16 columns per thread from 136; wider
+    # rows keep whole warps.  layout = (lanes per row, vectors per thread,
+    # rows per group)
     v = cake.cake_rmsnorm_bwd_select((4096, 1, H), deterministic=True)
-    if half:
-        assert (v["lanes_per_row"], v["vec_per_thread"], v["warps_per_row"], v["rows_per_group"]) == (16, 2, 1, 2), v
-    else:
-        assert v["lanes_per_row"] == 32 and not (v["vec_per_thread"] == 2 and v["rows_per_group"] == 2), v
+    assert (v["lanes_per_row"], v["vec_per_thread"], v["rows_per_group"]) == layout, v
+    assert v["warps_per_row"] == 1
 
 
 @pytest.mark.parametrize("shape,one", [((1, 1, 1536), True), ((16, 1, 1536), True), ((17, 1, 1536), False),
@@ -378,7 +379,9 @@ def test_tree_form_selection(cake):
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), deterministic=True, force_single=2)
     assert v["single"] == 2 and v["vec_per_thread"] == 2 and v["lanes_per_row"] == 16
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 128), deterministic=True, force_single=2)
-    assert v["single"] == 2 and v["vec_per_thread"] == 1 and v["lanes_per_row"] == 32
+    assert v["single"] == 2 and v["vec_per_thread"] == 1 and v["lanes_per_row"] == 16
+    v = cake.cake_rmsnorm_bwd_select((32768, 4, 64), deterministic=True, force_single=2)
+    assert v["single"] == 2 and v["vec_per_thread"] == 1 and v["lanes_per_row"] == 8
     v = cake.cake_rmsnorm_bwd_select((1000, 1, 512), deterministic=False, force_single=2)
     assert v["single"] == 2
     for H in (2048, 8192):  # 32 and 24 columns per thread: no tree form

@@ -175,10 +175,11 @@ def test_sweep_widths(cake, name):
     run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], full_dx=False, name=name)
 
 
-@pytest.mark.parametrize("T,H", [(65536, 200), (65536, 384), (32768, 640), (32768, 832)])
+@pytest.mark.parametrize("T,H", [(131072, 64), (65536, 128), (65536, 200), (65536, 384), (32768, 640), (32768, 832)])
 def test_narrow_row_layouts_at_size(cake, T, H):
-    # rows of half a warp (H = 200: part of each thread's second vector idle)
-    # and rows of one warp at 16, 24 and 32 columns per thread, at tens of
+    # rows of a quarter of a warp (H = 64), of half a warp (H = 128 at 8
+    # columns per thread; H = 200 at 16, part of each thread's second vector
+    # idle) and of one warp at 16, 24 and 32 columns per thread, at tens of
     # thousands of rows: dx of every row, dw of every column, both modes
     c = cake_inputs.plain_case(T, H, family="outlier", w_dtype=torch.float32, seed=T + H, device=DEV)
     run_workload(cake, c["x"], c["dy"], c["w"], c["eps"], name=f"T={T} H={H} outlier, w FP32")

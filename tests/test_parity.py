@@ -267,10 +267,12 @@ def check_bwd(cake, x, dy, w, eps, residual=None, dh=None, variants=VARIANTS, dw
 # and 333 x 200 leave part of each thread's second vector idle, 1001 x 256
 # spans several CTAs and ends on a tile whose second half-warp has no row;
 # rows of 384 to 1024 run on one warp at 16 to 32 columns per thread (61 x
-# 384 as one CTA, 700 x 512, 1003 x 640, 257 x 832 over several)
-BWD_SHAPES = [(1, 8), (2, 16), (3, 24), (2, 136), (37, 256), (333, 200), (1001, 256), (61, 384), (700, 512),
-              (1003, 640), (257, 832), (5, 520), (300, 1536), (129, 2048), (33, 4096), (17, 5120), (40, 6144),
-              (9, 8192), (1000, 2048)]
+# 384 as one CTA, 700 x 512, 1003 x 640, 257 x 832 over several); rows of at
+# most 64 columns on a quarter of a warp and of 72 to 128 on half a warp at 8
+# columns per thread (1003 x 64 and 517 x 128 end on a partly empty warp)
+BWD_SHAPES = [(1, 8), (2, 16), (3, 24), (1003, 64), (33, 72), (517, 128), (2, 136), (37, 256), (333, 200),
+              (1001, 256), (61, 384), (700, 512), (1003, 640), (257, 832), (5, 520), (300, 1536), (129, 2048),
+              (33, 4096), (17, 5120), (40, 6144), (9, 8192), (1000, 2048)]
 
 
 @pytest.mark.parametrize("T,H", BWD_SHAPES)
