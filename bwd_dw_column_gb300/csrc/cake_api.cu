@@ -146,12 +146,11 @@ static RowLayout row_layout(int H, Kind kind)
             return l;
     }
     const int nvec = H / 8;
-    // backward rows of at most 256 columns: part of a warp per row, so that
-    // one short butterfly reduces several rows and no lane idles -- 136 to
-    // 256 columns on half a warp at 16 columns per thread, 72 to 128 on half
-    // a warp at 8, at most 64 on a quarter of a warp at 8 (two or four rows
-    // per warp)
-    if (kind == kBwd && nvec <= 32 && tune().half != 0) {
+    // rows of at most 256 columns: part of a warp per row, so that one short
+    // butterfly reduces several rows and no lane idles -- 136 to 256 columns
+    // on half a warp at 16 columns per thread, 72 to 128 on half a warp at
+    // 8, at most 64 on a quarter of a warp at 8 (two or four rows per warp)
+    if (nvec <= 32 && tune().half != 0) {
         if (nvec > 16)
             return {2, 1, 16};
         return {1, 1, nvec > 8 ? 16 : 8};
@@ -365,13 +364,21 @@ static Plan make_plan(int H, uint32_t rows, int ntens, Kind kind, int single, in
     p.lo_bytes = lo_smem(kind, dwm, p.rl, p.groups);
     const size_t fixed = (size_t)kMiscBytes + weight_smem_bytes(H) + p.lo_bytes;
     int stages = per_cta > fixed ? (int)((per_cta - fixed) / stage) : 0;
-    // backward rows of one warp or half a warp at 16 or more columns per
-    // thread: at most four stages, fewer bytes in flight than would fit
-    // (GB300: [T, 24, 256] strided per-head views at T = 32768 192 us
-    // against 199-206 us with 3, 5, 6 or 8 stages; [T, 4, 256] 33.3 us
-    // against 34.3-35.0 us; H = 512, T = 131072 71.9 us against 73.6 us
-    // with 7 stages)
-    int want = kind == kBwd && p.rl.W == 1 && (p.rl.vpt >= 2 || p.rl.lanes) ? 4 : kMaxStages;
+    // Fewer bytes in flight than would fit run faster in places.  Backward
+    // rows of part of a warp, or of one warp at 16 or more columns per
+    // thread: at most four stages (GB300: [T, 24, 256] strided per-head views
+    // at T = 32768 192 us against 199-206 us with 3, 5, 6 or 8 stages;
+    // [T, 4, 256] 33.3 us against 34.3-35.0 us; H = 512, T = 131072 71.9 us
+    // against 73.6 us with 7 stages).  Forward rows of one warp or less: at
+    // most four stages too (H = 256, T = 131072 22.3 against 23.7 us; H =
+    // 512, T = 65536 22.8 against 24.0 us).  Wider forward rows keep what
+    // fits: three stages won at H = 2048 and 6144 but lost 4-6 % at H = 4096
+    // and on the residual route at H = 6144.
+    int want = kMaxStages;
+    if (kind == kBwd && p.rl.W == 1 && (p.rl.vpt >= 2 || p.rl.lanes))
+        want = 4;
+    if (kind == kFwd && p.rl.W == 1)
+        want = 4;
     if (tune().v[kind][3] >= 2)
         want = tune().v[kind][3];
     if (want < stages)
@@ -1335,7 +1342,7 @@ cake_status cake_rmsnorm_plan_occupancy(const cake_shape *shape, int backward, i
     const int threads = 32 * (plan.groups * plan.rl.W + 1);
     int n = 0;
     cudaError_t e = backward ? occupancy_bwd(plan.rl.vpt, plan.rl.W, plan.rpg, plan.rl.lanes ? plan.rl.lanes : 32, plan.single, plan.dwm, threads, plan.smem, &n)
-                             : occupancy_fwd(plan.rl.vpt, threads, plan.smem, &n);
+                             : occupancy_fwd(plan.rl.vpt, plan.rl.lanes ? plan.rl.lanes : 32, threads, plan.smem, &n);
     if (e != cudaSuccess)
         return CAKE_ERR_CUDA;
     *planned = plan.ctas_per_sm;

@@ -42,7 +42,11 @@ static cudaError_t status_ptr(int **out)
     return cudaSuccess;
 }
 
-template <int VPT>
+// LPR < 32: rows of LPR lanes (16 or 8), 32 / LPR per warp and row group --
+// lanes [s * LPR, (s + 1) * LPR) hold the group's row s of a tile, and one
+// log2(LPR)-step butterfly sums all of them; a thread's vectors are
+// k * LPR + lane % LPR.  Otherwise a row spans the group's W warps.
+template <int VPT, int LPR = 32>
 __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const __grid_constant__ FwdParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -66,6 +70,11 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
     const int gtid = wig * 32 + lane;
     const int nvec = L.nvec;
     const bool has_res = L.ntens == 2;
+    constexpr bool SUB = LPR < 32;
+    constexpr int RG = SUB ? 32 / LPR : 1; // rows a group owns per tile
+    const int sub = SUB ? lane / LPR : 0;
+    const int ltid = SUB ? lane % LPR : gtid;
+    const int vstride = SUB ? LPR : 32 * W;
 
     stage_weight(s, L, p.w, p.w_f32);
 
@@ -75,10 +84,13 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
     for (uint32_t it = 0; it < c.ntiles && !abort; ++it) {
         abort = !mbar_wait(smem_addr(&s.full[st]), ph, p.wait_ns);
         const uint8_t *stage = s.ring + st * s.stage_bytes;
-        const uint32_t r = c.r0 + it * c.tile_rows + gid;
-        if (r < c.r_end) { // uniform across the group
-            const uint4 *xs = reinterpret_cast<const uint4 *>(stage + gid * L.H * 2);
-            const uint4 *rsd = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + gid * L.H * 2);
+        const uint32_t gbase = c.r0 + it * c.tile_rows + gid * RG; // the group's first row
+        const uint32_t r = gbase + sub;                           // this thread's row
+        if (gbase < c.r_end) { // uniform across the group
+            const bool live = r < c.r_end; // all but the last rows of a tile of part-warp rows
+            const int tr = gid * RG + sub;
+            const uint4 *xs = reinterpret_cast<const uint4 *>(stage + tr * L.H * 2);
+            const uint4 *rsd = reinterpret_cast<const uint4 *>(stage + s.tens_bytes + tr * L.H * 2);
             // h = x, or bf16(x + residual): the FP32 sum of two BF16 values
             // rounds to the same BF16 value as their exact sum.  Sum of
             // squares: even / odd columns in the two lanes in the order of k
@@ -88,9 +100,9 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
             float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
+                const int v = k * vstride + ltid;
                 uint4 h = make_uint4(0, 0, 0, 0);
-                if (v < nvec) {
+                if (live && v < nvec) {
                     h = xs[v];
                     if (has_res) {
                         const uint4 rr = rsd[v];
@@ -109,7 +121,15 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
                 }
             }
             const float ss = __fadd_rn(ss2.x, ss2.y);
-            const float tot = group_sum(ss, s, L, gid, wig, lane, slot++, abort);
+            float tot = ss;
+            if constexpr (SUB) {
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1)
+                    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+                abort = __any_sync(0xffffffffu, abort);
+            } else {
+                tot = group_sum(ss, s, L, gid, wig, lane, slot++, abort);
+            }
             const float rs = 1.0f / sqrtf(__fadd_rn(__fmul_rn(tot, L.inv_h), p.eps));
             const float2 rs2 = make_float2(rs, rs);
 
@@ -119,8 +139,8 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
                                  : nullptr;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = k * 32 * W + gtid;
-                if (v < nvec && !abort) {
+                const int v = k * vstride + ltid;
+                if (live && v < nvec && !abort) {
                     float2 w2[4];
                     weight_pairs(s, L, v, w2);
                     uint32_t o[4];
@@ -132,7 +152,7 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
                         __stcs(reinterpret_cast<uint4 *>(hrow) + v, hraw[k]);
                 }
             }
-            if (gtid == 0 && !abort)
+            if (live && ltid == 0 && !abort)
                 p.rstd[r] = rs;
         }
         __syncwarp();
@@ -147,10 +167,10 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
         set_status(p.status, kStatusTimeout);
 }
 
-template <int VPT>
+template <int VPT, int LPR>
 static cudaError_t launch_fwd_vpt(const FwdParams &p, int ctas, size_t smem, cudaStream_t stream)
 {
-    auto kern = fwd_rows_kernel<VPT>;
+    auto kern = fwd_rows_kernel<VPT, LPR>;
     cudaError_t e = ensure_smem_attr((const void *)kern, smem);
     if (e != cudaSuccess)
         return e;
@@ -167,32 +187,46 @@ cudaError_t launch_fwd(const FwdParams &p, int vpt, int ctas, size_t smem, cudaS
         if (e != cudaSuccess)
             return e;
     }
+    const int lanes = q.L.lanes_per_row;
+    if (lanes != 32) {
+        // rows of part of a warp: one warp per group, 32 / lanes rows per group
+        if (q.L.warps_per_row != 1 || q.L.rows_per_group * lanes != 32)
+            return cudaErrorInvalidValue;
+        if (lanes == 16 && vpt == 1) return launch_fwd_vpt<1, 16>(q, ctas, smem, stream);
+        if (lanes == 16 && vpt == 2) return launch_fwd_vpt<2, 16>(q, ctas, smem, stream);
+        if (lanes == 8 && vpt == 1) return launch_fwd_vpt<1, 8>(q, ctas, smem, stream);
+        return cudaErrorInvalidValue;
+    }
     switch (vpt) {
-    case 1: return launch_fwd_vpt<1>(q, ctas, smem, stream);
-    case 2: return launch_fwd_vpt<2>(q, ctas, smem, stream);
-    case 3: return launch_fwd_vpt<3>(q, ctas, smem, stream);
-    case 4: return launch_fwd_vpt<4>(q, ctas, smem, stream);
+    case 1: return launch_fwd_vpt<1, 32>(q, ctas, smem, stream);
+    case 2: return launch_fwd_vpt<2, 32>(q, ctas, smem, stream);
+    case 3: return launch_fwd_vpt<3, 32>(q, ctas, smem, stream);
+    case 4: return launch_fwd_vpt<4, 32>(q, ctas, smem, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int VPT>
+template <int VPT, int LPR>
 static cudaError_t occ_fwd(int threads, size_t smem, int *n)
 {
-    auto kern = fwd_rows_kernel<VPT>;
+    auto kern = fwd_rows_kernel<VPT, LPR>;
     cudaError_t e = ensure_smem_attr((const void *)kern, smem);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
 }
 
-cudaError_t occupancy_fwd(int vpt, int threads, size_t smem, int *n)
+cudaError_t occupancy_fwd(int vpt, int lanes, int threads, size_t smem, int *n)
 {
+    if (lanes == 16 && vpt == 1) return occ_fwd<1, 16>(threads, smem, n);
+    if (lanes == 16 && vpt == 2) return occ_fwd<2, 16>(threads, smem, n);
+    if (lanes == 8 && vpt == 1) return occ_fwd<1, 8>(threads, smem, n);
+    if (lanes != 32) return cudaErrorInvalidValue;
     switch (vpt) {
-    case 1: return occ_fwd<1>(threads, smem, n);
-    case 2: return occ_fwd<2>(threads, smem, n);
-    case 3: return occ_fwd<3>(threads, smem, n);
-    case 4: return occ_fwd<4>(threads, smem, n);
+    case 1: return occ_fwd<1, 32>(threads, smem, n);
+    case 2: return occ_fwd<2, 32>(threads, smem, n);
+    case 3: return occ_fwd<3, 32>(threads, smem, n);
+    case 4: return occ_fwd<4, 32>(threads, smem, n);
     default: return cudaErrorInvalidValue;
     }
 }

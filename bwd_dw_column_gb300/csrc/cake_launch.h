@@ -20,7 +20,7 @@ cudaError_t launch_bwd_rows(const BwdParams &p, int vpt, int single, int dwm, in
 cudaError_t launch_dw_reduce(const ReduceParams &rp, cudaStream_t stream);
 
 // Resident CTAs per SM the runtime reports for a row kernel and launch shape.
-cudaError_t occupancy_fwd(int vpt, int threads, size_t smem, int *n);
+cudaError_t occupancy_fwd(int vpt, int lanes, int threads, size_t smem, int *n);
 cudaError_t occupancy_bwd(int vpt, int w, int rpg, int lanes, int single, int dwm, int threads, size_t smem, int *n);
 
 cudaError_t fwd_status(int *code, int clear);
