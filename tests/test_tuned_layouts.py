@@ -2,7 +2,8 @@
 
 The developer override CAKE_TUNE reaches kernel builds that no table plan
 uses today -- 8 columns per thread on 16 warps with two rows per group,
-16 columns per thread, 32 columns on two CTAs per SM.  The override is read
+16 columns per thread, 32 columns on two CTAs per SM, narrow rows on whole
+warps instead of part of one.  The override is read
 once per process, so each layout runs in a child process that applies the
 parity checks of tests/test_parity.py (dx against the oracle and the same
 bits across forms, calls and modes; dw within the budget) to a few shapes.
@@ -40,6 +41,7 @@ LAYOUTS = [
     ("vpt=1", [(300, 4096), (37, 3584)], (1, 2)),        # 16 warps per row, two rows per group
     ("vpt=2,fvpt=3", [(300, 2048), (45, 1024)], (2, 1)),  # 16 columns per thread
     ("vpt=4,groups=1,cps=2", [(300, 4096)], (4, 1)),     # 32 columns, two CTAs per SM
+    ("half=0", [(300, 256), (77, 64)], (1, 1)),           # rows of <= 256 columns on whole warps
 ]
 
 
