@@ -130,13 +130,8 @@ static RowLayout layout_for(int H, int vpt)
 // The row layout fixes which thread owns which columns and therefore the
 // reduction order of every per-row sum.  It depends on H (and on whether it
 // is the forward or the backward) alone, so dx, y and rstd are the same bits
-// whatever else the table picks.
-//   backward: 8 columns per thread up to H = 6144 except 24 for 4096 < H
-//     <= 5376 -- the backward keeps x, dy*w and the dw accumulators of its
-//     columns in registers, so few columns per thread leave room for many
-//     resident warps;
-//   forward: 16 columns per thread from H = 512 (fewer, longer rows per
-//     thread amortise the per-row reduction).
+// whatever else the table picks.  Both directions put rows of at most 256
+// columns on part of a warp; wider rows follow the rules below.
 static RowLayout row_layout(int H, Kind kind)
 {
     const int forced = tune().v[kind][0];
