@@ -175,7 +175,7 @@ def workload_plan(workload: str):
     try:
         import bwd_dw_column_gb300 as cake
         import cake_inputs
-        spec = cake_inputs.WORKLOADS[workload]
+        spec = cake_inputs.workload_spec(workload)
         shape = (spec["T"], spec.get("heads", 1), spec.get("H", 256))
         return cake.cake_rmsnorm_bwd_select(shape, spec["w_dtype"], deterministic=True,
                                             has_dh=spec["kind"] == "res")
@@ -414,7 +414,7 @@ class Workload:
     def __init__(self, cake, torch, name, dev, seed=0, accum=None, tokens=None):
         import cake_inputs
 
-        self.name, self.spec = name, dict(cake_inputs.WORKLOADS[name])
+        self.name, self.spec = name, dict(cake_inputs.workload_spec(name))
         if tokens:
             self.spec["T"] = tokens
         case = cake_inputs.make(name, seed=seed, device=dev, **({"T": tokens} if tokens else {}))
@@ -770,7 +770,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     name = args.workload or HEADLINE
-    spec = cake_inputs.WORKLOADS[name]
+    spec = cake_inputs.workload_spec(name)
     if spec["kind"] not in ("plain", "res"):
         raise SystemExit("the reference arm times plain and residual workloads")
     T, H = spec["T"], spec["H"]

@@ -173,9 +173,23 @@ for _H in SWEEP_H:
                                                 w_dtype=torch.float32, dy_std=1.0)
 
 
+# Shapes the pages do not name, for profiling layouts the named workloads do
+# not reach: narrow rows (per-head widths 64 and 128 as plain rows), which run
+# several to a warp.
+EXTRA_WORKLOADS = {
+    "h64_t524288": dict(kind="plain", T=524288, H=64, family="gauss", w_dtype=torch.bfloat16, dy_std=1.0),
+    "h128_t262144": dict(kind="plain", T=262144, H=128, family="gauss", w_dtype=torch.bfloat16, dy_std=1.0),
+}
+
+
+def workload_spec(name: str) -> dict:
+    """The spec of a named workload: one of ``WORKLOADS``, else ``EXTRA_WORKLOADS``."""
+    return WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name]
+
+
 def make(name: str, seed: int = 0, device="cpu", **overrides) -> dict:
-    """Build one named workload (``WORKLOADS``), optionally with overridden sizes."""
-    spec = dict(WORKLOADS[name])
+    """Build one named workload (``workload_spec``), optionally with overridden sizes."""
+    spec = dict(workload_spec(name))
     spec.update(overrides)
     kind = spec.pop("kind")
     if kind == "plain":
