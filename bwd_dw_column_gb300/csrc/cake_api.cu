@@ -72,7 +72,8 @@ struct Tune {
     int v[2][6] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}}; // [kind][vpt, groups, cps, stages, rpg, form+1]
     int cluster = 0;                                         // cluster form: CTAs per cluster
     int one_cta_elems = 0;                                   // backward: one CTA up to rows * H elements
-    int half = -1;                                           // backward rows of part of a warp: 0 off
+    int half = -1;                                           // rows of part of a warp: 0 off
+    int narrow = -1;                                         // rows of at most 128 columns: 0 at 8 columns per thread
     int rslices = 0;                                         // the pair's reduce: partial ranges per column and warp
 };
 
@@ -100,6 +101,8 @@ static Tune parse_tune(const char *t)
             r.one_cta_elems = val;
         if (klen == 4 && strncmp(p, "half", 4) == 0 && (val == 0 || val == 1))
             r.half = val;
+        if (klen == 6 && strncmp(p, "narrow", 6) == 0 && (val == 0 || val == 1))
+            r.narrow = val;
         if (klen == 7 && strncmp(p, "rslices", 7) == 0 && (val == 1 || val == 2 || val == 4 || val == 8))
             r.rslices = val;
         const char *comma = strchr(eq, ',');
@@ -141,14 +144,20 @@ static RowLayout row_layout(int H, Kind kind)
             return l;
     }
     const int nvec = H / 8;
-    // rows of at most 256 columns: part of a warp per row, so that one short
-    // butterfly reduces several rows and no lane idles -- 136 to 256 columns
-    // on half a warp at 16 columns per thread, 72 to 128 on half a warp at
-    // 8, at most 64 on a quarter of a warp at 8 (two or four rows per warp)
+    // rows of at most 256 columns: part of a warp per row at 16 columns per
+    // thread, so that one short butterfly reduces several rows and no lane
+    // idles -- 136 to 256 columns on half a warp, 72 to 128 on a quarter, at
+    // most 64 on an eighth (two, four or eight rows per warp).  GB300, 16
+    // against 8 columns per thread on twice the lanes: H = 64, T = 524288
+    // backward pair 37.2 vs 39.3 us, forward 22.7 vs 27.0 us; H = 128, T =
+    // 262144 36.9 vs 40.3 us and 21.8 vs 27.1 us.  (Rows of one warp at 8
+    // columns per thread took 123 and 67 us for the backward.)
     if (nvec <= 32 && tune().half != 0) {
         if (nvec > 16)
             return {2, 1, 16};
-        return {1, 1, nvec > 8 ? 16 : 8};
+        if (tune().narrow == 0)
+            return {1, 1, nvec > 8 ? 16 : 8};
+        return {2, 1, nvec > 8 ? 8 : 4};
     }
     if (nvec <= 32)
         return {1, 1};

@@ -90,18 +90,21 @@ __global__ void __launch_bounds__(32 * kReduceWarps) dw_reduce_kernel(const __gr
 // ------------------------------------------------------------------ launch
 
 // The row build of a layout: rows of part of a warp -- 5 half a warp at
-// two 8-column vectors per thread, 6 half a warp at one, 7 a quarter at one
-// (one warp per group, 32 / lanes rows per warp and group); 1 two rows per
+// two 8-column vectors per thread, 6 half a warp at one, 7 a quarter at one,
+// 8 a quarter at two, 9 an eighth at two (one warp per group, 32 / lanes rows
+// per warp and group); 1 two rows per
 // group of one vector per thread; 4 rows of one warp at 8 columns per
 // thread; 0 otherwise; -1 for a combination no build serves.
 static int row_build(int vpt, int W, int rpg, int lanes, int threads)
 {
-    if (lanes == 16 || lanes == 8) {
+    if (lanes == 16 || lanes == 8 || lanes == 4) {
         if (W != 1 || rpg != 32 / lanes || threads > kMaxThreadsFor(vpt))
             return -1;
         if (lanes == 16)
             return vpt == 2 ? 5 : vpt == 1 ? 6 : -1;
-        return vpt == 1 ? 7 : -1;
+        if (lanes == 8)
+            return vpt == 1 ? 7 : vpt == 2 ? 8 : -1;
+        return vpt == 2 ? 9 : -1;
     }
     if (lanes != 32)
         return -1;

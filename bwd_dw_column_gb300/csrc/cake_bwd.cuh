@@ -692,14 +692,16 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
 // group (one group of up to 16 warps and the producer per CTA), keeping x and
 // dy*w of both rows in registers; 4 one row per group for rows of one warp
 // (H <= 256), with that width known to the compiler; rows of part of a warp:
-// 5 (VPT = 2) and 6 (VPT = 1) half a warp, two rows per warp; 7 (VPT = 1) a
-// quarter, four rows per warp.  The bounds cap the registers a thread may use
+// 5 (VPT = 2) and 6 (VPT = 1) half a warp, two rows per warp; 7 (VPT = 1)
+// and 8 (VPT = 2) a quarter, four rows per warp; 9 (VPT = 2) an eighth,
+// eight rows per warp.  The bounds cap the registers a thread may use
 // so that the largest CTA fits: 72 (26 warps), 96 (17 warps), 128 (13 warps).
 template <int VPT, int DWM, int FORM, int RB>
 __global__ void __launch_bounds__(RB == 1 ? kMaxThreadsR2 : kMaxThreadsFor(VPT), 1)
     bwd_rows_kernel(const __grid_constant__ BwdParams p)
 {
-    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4 || RB >= 5, RB == 5 || RB == 6 ? 16 : RB == 7 ? 8 : 32>(p);
+    bwd_rows<VPT, DWM, FORM, RB == 1 ? 2 : 1, true, RB == 4 || RB >= 5,
+             RB == 5 || RB == 6 ? 16 : RB == 7 || RB == 8 ? 8 : RB == 9 ? 4 : 32>(p);
 }
 
 // ------------------------------------------------------------------ launch
@@ -794,6 +796,8 @@ cudaError_t launch_bwd_form(const BwdParams &p, int vpt, int rb, int dwm, int ct
     if (vpt == 2 && rb == 5) return launch_dwm<2, FORM, 5>(p, dwm, ctas, smem, stream);
     if (vpt == 1 && rb == 6) return launch_dwm<1, FORM, 6>(p, dwm, ctas, smem, stream);
     if (vpt == 1 && rb == 7) return launch_dwm<1, FORM, 7>(p, dwm, ctas, smem, stream);
+    if (vpt == 2 && rb == 8) return launch_dwm<2, FORM, 8>(p, dwm, ctas, smem, stream);
+    if (vpt == 2 && rb == 9) return launch_dwm<2, FORM, 9>(p, dwm, ctas, smem, stream);
     if constexpr (FORM == kFormTree) {
         if (vpt == 2 && rb == 0) return launch_dwm<2, FORM, 0>(p, dwm, ctas, smem, stream);
         return vpt == 1 && rb != 1 ? launch_dwm<1, FORM, 0>(p, dwm, ctas, smem, stream) : cudaErrorInvalidValue;
@@ -817,6 +821,8 @@ cudaError_t occ_bwd_form(int vpt, int rb, int dwm, int threads, size_t smem, int
     if (vpt == 2 && rb == 5) return occ_dwm<2, FORM, 5>(dwm, threads, smem, n);
     if (vpt == 1 && rb == 6) return occ_dwm<1, FORM, 6>(dwm, threads, smem, n);
     if (vpt == 1 && rb == 7) return occ_dwm<1, FORM, 7>(dwm, threads, smem, n);
+    if (vpt == 2 && rb == 8) return occ_dwm<2, FORM, 8>(dwm, threads, smem, n);
+    if (vpt == 2 && rb == 9) return occ_dwm<2, FORM, 9>(dwm, threads, smem, n);
     if constexpr (FORM == kFormTree) {
         if (vpt == 2 && rb == 0) return occ_dwm<2, FORM, 0>(dwm, threads, smem, n);
         return vpt == 1 && rb != 1 ? occ_dwm<1, FORM, 0>(dwm, threads, smem, n) : cudaErrorInvalidValue;

@@ -42,7 +42,7 @@ static cudaError_t status_ptr(int **out)
     return cudaSuccess;
 }
 
-// LPR < 32: rows of LPR lanes (16 or 8), 32 / LPR per warp and row group --
+// LPR < 32: rows of LPR lanes (16, 8 or 4), 32 / LPR per warp and row group --
 // lanes [s * LPR, (s + 1) * LPR) hold the group's row s of a tile, and one
 // log2(LPR)-step butterfly sums all of them; a thread's vectors are
 // k * LPR + lane % LPR.  Otherwise a row spans the group's W warps.
@@ -195,6 +195,8 @@ cudaError_t launch_fwd(const FwdParams &p, int vpt, int ctas, size_t smem, cudaS
         if (lanes == 16 && vpt == 1) return launch_fwd_vpt<1, 16>(q, ctas, smem, stream);
         if (lanes == 16 && vpt == 2) return launch_fwd_vpt<2, 16>(q, ctas, smem, stream);
         if (lanes == 8 && vpt == 1) return launch_fwd_vpt<1, 8>(q, ctas, smem, stream);
+        if (lanes == 8 && vpt == 2) return launch_fwd_vpt<2, 8>(q, ctas, smem, stream);
+        if (lanes == 4 && vpt == 2) return launch_fwd_vpt<2, 4>(q, ctas, smem, stream);
         return cudaErrorInvalidValue;
     }
     switch (vpt) {
@@ -221,6 +223,8 @@ cudaError_t occupancy_fwd(int vpt, int lanes, int threads, size_t smem, int *n)
     if (lanes == 16 && vpt == 1) return occ_fwd<1, 16>(threads, smem, n);
     if (lanes == 16 && vpt == 2) return occ_fwd<2, 16>(threads, smem, n);
     if (lanes == 8 && vpt == 1) return occ_fwd<1, 8>(threads, smem, n);
+    if (lanes == 8 && vpt == 2) return occ_fwd<2, 8>(threads, smem, n);
+    if (lanes == 4 && vpt == 2) return occ_fwd<2, 4>(threads, smem, n);
     if (lanes != 32) return cudaErrorInvalidValue;
     switch (vpt) {
     case 1: return occ_fwd<1, 32>(threads, smem, n);

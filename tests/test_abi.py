@@ -108,14 +108,14 @@ def test_row_layout_depends_on_h_alone(cake):
         assert len(layouts) == 1, (H, layouts)
 
 
-@pytest.mark.parametrize("H,layout", [(8, (8, 1, 4)), (64, (8, 1, 4)), (72, (16, 1, 2)), (128, (16, 1, 2)),
+@pytest.mark.parametrize("H,layout", [(8, (4, 2, 8)), (64, (4, 2, 8)), (72, (8, 2, 4)), (128, (8, 2, 4)),
                                       (136, (16, 2, 2)), (200, (16, 2, 2)), (256, (16, 2, 2)), (264, (32, 2, 1)),
                                       (512, (32, 2, 1))])
 def test_part_warp_rows(cake, H, layout):
-    # backward rows of at most 256 columns take part of a warp: a quarter up
-    # to 64 columns, a half above, at 16 columns per thread from 136; wider
-    # rows keep whole warps.  layout = (lanes per row, vectors per thread,
-    # rows per group)
+    # rows of at most 256 columns take part of a warp at 16 columns per
+    # thread: an eighth up to 64 columns, a quarter to 128, a half to 256;
+    # wider rows keep whole warps.  layout = (lanes per row, vectors per
+    # thread, rows per group)
     v = cake.cake_rmsnorm_bwd_select((4096, 1, H), deterministic=True)
     assert (v["lanes_per_row"], v["vec_per_thread"], v["rows_per_group"]) == layout, v
     assert v["warps_per_row"] == 1
@@ -379,9 +379,9 @@ def test_tree_form_selection(cake):
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 256), deterministic=True, force_single=2)
     assert v["single"] == 2 and v["vec_per_thread"] == 2 and v["lanes_per_row"] == 16
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 128), deterministic=True, force_single=2)
-    assert v["single"] == 2 and v["vec_per_thread"] == 1 and v["lanes_per_row"] == 16
+    assert v["single"] == 2 and v["vec_per_thread"] == 2 and v["lanes_per_row"] == 8
     v = cake.cake_rmsnorm_bwd_select((32768, 4, 64), deterministic=True, force_single=2)
-    assert v["single"] == 2 and v["vec_per_thread"] == 1 and v["lanes_per_row"] == 8
+    assert v["single"] == 2 and v["vec_per_thread"] == 2 and v["lanes_per_row"] == 4
     v = cake.cake_rmsnorm_bwd_select((1000, 1, 512), deterministic=False, force_single=2)
     assert v["single"] == 2
     for H in (2048, 8192):  # 32 and 24 columns per thread: no tree form

@@ -3,7 +3,7 @@
 The developer override CAKE_TUNE reaches kernel builds that no table plan
 uses today -- 8 columns per thread on 16 warps with two rows per group,
 16 columns per thread, 32 columns on two CTAs per SM, narrow rows on whole
-warps instead of part of one.  The override is read
+warps instead of part of one, or on part of one at 8 columns per thread.  The override is read
 once per process, so each layout runs in a child process that applies the
 parity checks of tests/test_parity.py (dx against the oracle and the same
 bits across forms, calls and modes; dw within the budget) to a few shapes.
@@ -42,6 +42,7 @@ LAYOUTS = [
     ("vpt=2,fvpt=3", [(300, 2048), (45, 1024)], (2, 1)),  # 16 columns per thread
     ("vpt=4,groups=1,cps=2", [(300, 4096)], (4, 1)),     # 32 columns, two CTAs per SM
     ("half=0", [(300, 256), (77, 64)], (1, 1)),           # rows of <= 256 columns on whole warps
+    ("narrow=0", [(1003, 64), (77, 8)], (1, 4)),         # quarter-warp rows at 8 columns per thread
 ]
 
 
