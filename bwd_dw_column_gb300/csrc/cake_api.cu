@@ -161,15 +161,17 @@ static RowLayout row_layout(int H, Kind kind)
     }
     if (nvec <= 32)
         return {1, 1};
-    // backward rows of 264 to 1024 columns: one warp per row at the fewest
-    // vectors per thread that cover it.  It has as many vector slots as 8
-    // columns per thread on that many warps, but no cross-warp barrier per
-    // row, and 16 to 32 columns share each thread's per-row work (GB300,
-    // deterministic pair, against 8 columns per thread on 2-4 warps: T =
-    // 65536, H = 320 39.2 vs 41.7 us, 384 39.6 vs 42.2, 512 40.8 vs 43.3,
-    // 576 49.4 vs 55.9, 640 49.9 vs 56.5, 704 50.9 vs 57.4, 832 63.7 vs
-    // 69.6; T = 131072, H = 640 88.3 vs 99.2, 832 113.8 vs 127.1)
-    if (kind == kBwd && nvec <= 128)
+    // rows of 264 to 1024 columns: one warp per row at the fewest vectors
+    // per thread that cover it.  It has as many vector slots as 8 columns per
+    // thread on that many warps, but no cross-warp barrier per row, and 16 to
+    // 32 columns share each thread's per-row work (GB300, T = 65536 unless
+    // noted.  Backward pair, against 8 columns per thread on 2-4 warps: H =
+    // 320 39.2 vs 41.7 us, 384 39.6 vs 42.2, 512 40.8 vs 43.3, 576 49.4 vs
+    // 55.9, 640 49.9 vs 56.5, 704 50.9 vs 57.4, 832 63.7 vs 69.6; T = 131072,
+    // H = 640 88.3 vs 99.2, 832 113.8 vs 127.1.  Forward, against 16 columns
+    // per thread on 2 warps: H = 576 27.0 vs 38.1 us, 640 28.1 vs 38.6, 768
+    // 31.3 vs 39.3, 832 34.6 vs 40.1, 1024 42.1 vs 43.2)
+    if (nvec <= 128)
         return {(nvec + 31) / 32, 1};
     // backward, 24 or 32 columns per thread where the row splits into W warps
     // with W dividing 12 and enough of the lanes' vectors in use: an SM then

@@ -134,10 +134,12 @@ def check_fwd(cake, x, w, eps, residual=None):
     return r64, hn
 
 
-# rows of at most 256 columns run on part of a warp (1003 x 64: four rows per
-# warp, the last warp partly empty; 517 x 128 and 333 x 200: two)
-FWD_SHAPES = [(1, 8), (3, 24), (1003, 64), (517, 128), (333, 200), (37, 256), (5, 520), (300, 1536), (129, 2048),
-              (33, 4096), (17, 5120), (40, 6144), (9, 8192)]
+# rows of at most 256 columns run on part of a warp (1003 x 64: eight rows
+# per warp, the last warp partly empty; 517 x 128: four; 333 x 200: two);
+# rows of 264 to 1024 on one warp at 16 to 32 columns per thread (5 x 520,
+# 1001 x 640, 77 x 1024)
+FWD_SHAPES = [(1, 8), (3, 24), (1003, 64), (517, 128), (333, 200), (37, 256), (5, 520), (1001, 640), (77, 1024),
+              (300, 1536), (129, 2048), (33, 4096), (17, 5120), (40, 6144), (9, 8192)]
 
 
 @pytest.mark.parametrize("T,H", FWD_SHAPES)
