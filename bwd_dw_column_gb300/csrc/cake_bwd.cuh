@@ -44,14 +44,21 @@
 
 namespace cake {
 
+// Where slot m = 4 v + q of a row group's partial sits in shared memory (in
+// float4 units from the group's base): the four slots of vector v together,
+// permuted by bits 1-2 of v, so that eight lanes on consecutive vectors
+// writing one q, and eight lanes on consecutive slots reading, each touch
+// eight different 16-byte bank quads (GB300: 0.3-0.5 us off a one-row call).
+__device__ __forceinline__ int comb_slot(int v, int q) { return 4 * v + (q ^ ((v >> 1) & 3)); }
+
 // Slot m = 4 v + q of the CTA partial (columns 8 v + 2 q and the next one,
 // float4 (hi.x, lo.x, hi.y, lo.y)) summed over the row groups' partials in
-// shared memory (at shared address comb, [group][q][vector]) in group order,
+// shared memory (at shared address comb, [group][comb_slot]) in group order,
 // four groups' loads in flight at a time.
 __device__ __forceinline__ float4 slot_sum(uint32_t comb, int nvec, int groups, int m)
 {
     const int v = m >> 2, q = m & 3;
-    const uint32_t base = comb + 16u * (uint32_t)(q * nvec + v);
+    const uint32_t base = comb + 16u * (uint32_t)comb_slot(v, q);
     const uint32_t gstride = 64u * (uint32_t)nvec;
     float4 a = ld_shared_f4(base);
     for (int g0 = 1; g0 < groups; g0 += 4) {
@@ -73,10 +80,8 @@ __device__ __forceinline__ float4 slot_sum(uint32_t comb, int nvec, int groups, 
 
 // The pair's CTA partial to global memory (or, for a pair of one CTA, dw
 // itself: hi + lo rounded once, the bits the reduce of one partial gives).
-// Not inlined, so that none of its addressing is hoisted into the row loop,
-// whose widest builds use every register a thread may have.
-static __device__ __noinline__ void emit_pair_partial(uint32_t comb, int nvec, int groups, int nthr, float4 *dst,
-                                                      float2 *dw, int direct)
+__device__ __forceinline__ void emit_pair_body(uint32_t comb, int nvec, int groups, int nthr, float4 *dst, float2 *dw,
+                                               int direct)
 {
     for (int m = (int)threadIdx.x; m < 4 * nvec; m += nthr) {
         const float4 a = slot_sum(comb, nvec, groups, m);
@@ -85,6 +90,16 @@ static __device__ __noinline__ void emit_pair_partial(uint32_t comb, int nvec, i
         else
             dst[m] = a;
     }
+}
+// The same as a called function, for the build whose row loop uses every
+// register a thread may have (32 columns per thread with Kahan sums): inlined
+// there, its addressing is hoisted into the loop and spills.  Elsewhere the
+// call costs more than it saves (GB300: about 0.5 us of a one-row call, the
+// stack frame's round trip).
+static __device__ __noinline__ void emit_pair_partial(uint32_t comb, int nvec, int groups, int nthr, float4 *dst,
+                                                      float2 *dw, int direct)
+{
+    emit_pair_body(comb, nvec, groups, nthr, dst, dw, direct);
 }
 
 template <int VPT, int DWM, int FORM, int R2, bool KEEP, bool W1, int LPR = 32>
@@ -449,11 +464,11 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     }
 
     // ---- the CTA partial.  Every row group writes its partial to shared
-    // memory ([group][q][vector] float4 (hi.x, lo.x, hi.y, lo.y): a warp's
-    // lanes touch consecutive 16-byte slots, free of bank conflicts), then
-    // every consumer thread sums whole slots over the groups in group order
-    // -- slot m = 4 v + q holds columns 8 v + 2 q and the next one -- so the
-    // combine is spread over the CTA instead of left to one group.
+    // memory ([group][comb_slot(v, q)] float4 (hi.x, lo.x, hi.y, lo.y), free
+    // of bank conflicts), then every consumer thread sums whole slots over
+    // the groups in group order -- slot m = 4 v + q holds columns 8 v + 2 q
+    // and the next one -- so the combine is spread over the CTA instead of
+    // left to one group.
     consumer_sync(L);
     float4 *comb = reinterpret_cast<float4 *>(s.ring);
     const int ncol = nvec * 8;
@@ -465,7 +480,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         if (owner && v < nvec)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                comb[(gid * 4 + q) * nvec + v] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
+                comb[gid * nslot + comb_slot(v, q)] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
     }
     consumer_sync(L);
     // calls emit(m, slot) for each of this thread's slots of the CTA partial
@@ -538,8 +553,11 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     if constexpr (FORM == kFormPair) {
         // the CTA partial, or for a pair of one CTA dw itself (the reduce of
         // a single partial would give the same bits, hi + lo rounded once)
-        emit_pair_partial(smem_addr(comb), nvec, L.groups, nthr, reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol),
-                          reinterpret_cast<float2 *>(p.dw), p.direct_dw);
+        float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);
+        if constexpr (VPT >= 4 && DWM == CAKE_DWM_KAHAN)
+            emit_pair_partial(smem_addr(comb), nvec, L.groups, nthr, dst, reinterpret_cast<float2 *>(p.dw), p.direct_dw);
+        else
+            emit_pair_body(smem_addr(comb), nvec, L.groups, nthr, dst, reinterpret_cast<float2 *>(p.dw), p.direct_dw);
         // the reduce may launch once every CTA has written its partial (GB300:
         // 1-2 us faster at T = 4096 than a trigger before the group combine)
         pdl_launch_dependents();
