@@ -474,10 +474,17 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     const int ncol = nvec * 8;
     const int nslot = 4 * nvec;
     const int nthr = consumer_warps * 32;
+    // The row groups that owned a row of this CTA.  Every sum starts at +0
+    // and round-to-nearest never turns a sum into -0, so the other groups'
+    // partials are +0 and adding them changes no bit: the combine reads the
+    // live groups only, in the same order (GB300: 0.3-0.5 us off a one-row
+    // call, where one group of several is live).
+    const uint32_t crows = c.r_end > c.r0 ? c.r_end - c.r0 : 0u;
+    const int live = max(1, min(L.groups, (int)((crows + (uint32_t)RG - 1u) / (uint32_t)RG)));
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * vstride + ltid;
-        if (owner && v < nvec)
+        if (owner && v < nvec && gid < live)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 comb[gid * nslot + comb_slot(v, q)] = make_float4(hi[k][q].x, lo[k][q].x, hi[k][q].y, lo[k][q].y);
@@ -486,7 +493,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
     // calls emit(m, slot) for each of this thread's slots of the CTA partial
     auto for_each_slot = [&](auto &&emit) {
         for (int m = (int)threadIdx.x; m < nslot; m += nthr)
-            emit(m, slot_sum(smem_addr(comb), nvec, L.groups, m));
+            emit(m, slot_sum(smem_addr(comb), nvec, live, m));
     };
 
     if constexpr (FORM == kFormCluster) {
@@ -555,9 +562,9 @@ __device__ __forceinline__ void bwd_rows(const BwdParams &p)
         // a single partial would give the same bits, hi + lo rounded once)
         float4 *dst = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * ncol);
         if constexpr (VPT >= 4 && DWM == CAKE_DWM_KAHAN)
-            emit_pair_partial(smem_addr(comb), nvec, L.groups, nthr, dst, reinterpret_cast<float2 *>(p.dw), p.direct_dw);
+            emit_pair_partial(smem_addr(comb), nvec, live, nthr, dst, reinterpret_cast<float2 *>(p.dw), p.direct_dw);
         else
-            emit_pair_body(smem_addr(comb), nvec, L.groups, nthr, dst, reinterpret_cast<float2 *>(p.dw), p.direct_dw);
+            emit_pair_body(smem_addr(comb), nvec, live, nthr, dst, reinterpret_cast<float2 *>(p.dw), p.direct_dw);
         // the reduce may launch once every CTA has written its partial (GB300:
         // 1-2 us faster at T = 4096 than a trigger before the group combine)
         pdl_launch_dependents();
