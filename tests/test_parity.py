@@ -276,7 +276,9 @@ def check_bwd(cake, x, dy, w, eps, residual=None, dh=None, variants=VARIANTS, dw
 # columns per thread (1003 x 64 and 517 x 128 end on a partly empty warp)
 BWD_SHAPES = [(1, 8), (2, 16), (3, 24), (1003, 64), (33, 72), (517, 128), (2, 136), (37, 256), (333, 200),
               (1001, 256), (61, 384), (700, 512), (1003, 640), (257, 832), (5, 520), (300, 1536), (129, 2048),
-              (33, 4096), (17, 5120), (40, 6144), (9, 8192), (1000, 2048)]
+              (33, 4096), (17, 5120), (40, 6144), (9, 8192), (1000, 2048),
+              # one CTA with fewer rows than row groups: the combine reads only the live groups
+              (1, 1536), (2, 2048), (2, 4096), (1, 6144), (5, 1536)]
 
 
 @pytest.mark.parametrize("T,H", BWD_SHAPES)
