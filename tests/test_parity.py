@@ -297,6 +297,42 @@ def test_bwd_families(cake, family, T, H):
     check_bwd(cake, c["x"], c["dy"], c["w"], c["eps"], variants=[(0, 0), (0, 1), (1, 1), (3, 3)])
 
 
+@pytest.mark.parametrize("H", [8, 64, 256, 520, 1536, 2048, 4096, 6144, 8192])
+def test_one_row_dw_is_one_rounding(cake, H):
+    """One row: dw_j = dy_j * x_j * rstd with a single rounding to FP32.  The
+    BF16 product is exact in FP32, the multiply-add by rstd rounds once, and
+    every accumulation form and every form of the column reduction leaves that
+    value as it is.  FP64 holds the exact product (16 + 24 significant bits),
+    so the equality is bit for bit.  The CTA's other row groups own no row:
+    any bit of theirs in the group combine, or a slot read from the wrong
+    place, breaks it."""
+    c = cake_inputs.plain_case(1, H, seed=H + 5)
+    x, dy, w = c["x"], c["dy"], c["w"]
+    rin, _ = oracle_bwd_inputs(x, w, c["eps"])
+    want = (rows_f64(dy)[0] * rows_f64(x)[0] * np.float64(rin[0])).astype(np.float32)
+    x_d, dy_d, w_d = x.to(DEV), dy.to(DEV), w.to(DEV)
+    r_d = torch.from_numpy(rin).to(DEV)
+    runs = [("table det", lambda: cake.cake_rmsnorm_bwd(dy_d, x_d, r_d, w_d, None, deterministic=True)),
+            ("table nondet", lambda: cake.cake_rmsnorm_bwd(dy_d, x_d, r_d, w_d, None, deterministic=False))]
+    for single, acc in VARIANTS:
+        runs.append((f"form {single} accum {acc}",
+                     lambda single=single, acc=acc: cake.cake_rmsnorm_bwd_forced(
+                         dy_d, x_d, r_d, w_d, None, deterministic=single != 1, force_single=single, force_accum=acc)))
+    checked = 0
+    for name, fn in runs:
+        try:
+            _, dw = fn()
+        except cake.CakeError as e:
+            assert e.status == 2, name  # the tree form exists for some layouts only
+            continue
+        torch.cuda.synchronize()
+        got = dw.cpu().numpy()
+        bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
+        assert bad.size == 0, f"{name}: {bad.size} columns differ, first {bad[0]}: {got[bad[0]]!r} != {want[bad[0]]!r}"
+        checked += 1
+    assert checked >= 18
+
+
 @pytest.mark.parametrize("T,H", [(3, 256), (300, 1536), (77, 6144)])
 def test_bwd_residual(cake, T, H):
     c = cake_inputs.residual_case(T, H, seed=H + 1)
