@@ -77,6 +77,14 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
     const int vstride = SUB ? LPR : 32 * W;
 
     stage_weight(s, L, p.w, p.w_f32);
+    // a thread's columns are the same on every row: its weights stay in
+    // registers where the build has room for them
+    constexpr bool kWreg = VPT <= 2;
+    float2 wreg[kWreg ? VPT : 1][4];
+    if constexpr (kWreg)
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            weight_pairs(s, L, k * vstride + ltid < nvec ? k * vstride + ltid : 0, wreg[k]);
 
     bool abort = false;
     uint32_t slot = 0;
@@ -142,7 +150,13 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
                 const int v = k * vstride + ltid;
                 if (live && v < nvec && !abort) {
                     float2 w2[4];
-                    weight_pairs(s, L, v, w2);
+                    if constexpr (kWreg) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            w2[q] = wreg[k][q];
+                    } else {
+                        weight_pairs(s, L, v, w2);
+                    }
                     uint32_t o[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
