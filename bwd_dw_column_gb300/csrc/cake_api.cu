@@ -254,7 +254,7 @@ static size_t lo_smem(Kind kind, int dwm, const RowLayout &rl, int groups)
 // a GPU test checks it against the occupancy the runtime reports.
 static int kernel_regs(Kind kind, int vpt, int rpg, int dwm, int lanes)
 {
-    static const int fwd[5] = {0, 52, 72, 80, 96};
+    static const int fwd[5] = {0, 52, 72, 96, 96};
     if (kind == kFwd)
         return fwd[vpt];
     if (lanes && vpt == 2)

@@ -78,8 +78,10 @@ __global__ void __launch_bounds__(kMaxThreadsFor(VPT), 1) fwd_rows_kernel(const 
 
     stage_weight(s, L, p.w, p.w_f32);
     // a thread's columns are the same on every row: its weights stay in
-    // registers where the build has room for them
-    constexpr bool kWreg = VPT <= 2;
+    // registers up to 24 columns per thread (GB300, T = 65536: H = 640 and
+    // 8192 5 %, H = 4096 4 %, H = 6144 2 % faster; H = 5120 1 % slower, where
+    // 24 columns on 7 warps then fit two CTAs per SM instead of three)
+    constexpr bool kWreg = VPT <= 3;
     float2 wreg[kWreg ? VPT : 1][4];
     if constexpr (kWreg)
 #pragma unroll
