@@ -157,15 +157,46 @@ def measured_peak():
 HOST_ONLY_SOURCES = ("cake_api.cu",)
 
 
+def canonical_source(text: str) -> str:
+    """C/C++/CUDA source without its comments, blank lines and the spaces
+    around each line: what the compiler turns into code.  An edit to a
+    comment or to indentation leaves it as it is; any other edit changes it.
+    String and character literals are kept whole (a // inside one is code)."""
+    out = []
+    i, n = 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and i + 1 < n and text[i + 1] == "/":
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif c == "/" and i + 1 < n and text[i + 1] == "*":
+            j = text.find("*/", i + 2)
+            end = n if j < 0 else j + 2
+            out.append("\n" * text.count("\n", i, end) or " ")
+            i = end
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c and text[j] != "\n":
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = (ln.strip() for ln in "".join(out).split("\n"))
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash():
-    """Hash of the kernel sources (every csrc file but the host-only ones)."""
+    """Hash of the kernel sources (every csrc file but the host-only ones),
+    taken over their canonical form, so that comments do not count."""
     csrc = os.path.join(ROOT, "bwd_dw_column_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f in HOST_ONLY_SOURCES:
             continue
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + canonical_source(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -94,8 +94,8 @@ __device__ __forceinline__ void emit_pair_body(uint32_t comb, int nvec, int grou
 // The same as a called function, for the build whose row loop uses every
 // register a thread may have (32 columns per thread with Kahan sums): inlined
 // there, its addressing is hoisted into the loop and spills.  Elsewhere the
-// call costs more than it saves (GB300: about 0.5 us of a one-row call, the
-// stack frame's round trip).
+// call costs more than it saves (GB300: about 0.5 us of a one-row call,
+// although ptxas gives the called function no stack frame).
 static __device__ __noinline__ void emit_pair_partial(uint32_t comb, int nvec, int groups, int nthr, float4 *dst,
                                                       float2 *dw, int direct)
 {

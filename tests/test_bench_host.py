@@ -95,6 +95,22 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.traffic_record("bwd_rows_kernel", "missing") is None
 
 
+def test_source_hash_ignores_comments_only():
+    # the kernel-source hash that keys the traffic records is taken over the
+    # sources without comments: a comment edit keeps the records, any edit
+    # to code (a literal included) makes them stale
+    import bench
+    base = 'x = 1; // why\n/* how\n   more */ y = "s//t"; char c = \'/\';\n'
+    same = 'x = 1;    // another reason\n\n/* two\n   lines */ y = "s//t"; char c = \'/\';  \n'
+    assert bench.canonical_source(base) == bench.canonical_source(same)
+    for changed in ('x = 2; // why\n/* how\n   more */ y = "s//t"; char c = \'/\';\n',
+                    'x = 1; // why\n/* how\n   more */ y = "s/t"; char c = \'/\';\n',
+                    'x = 1; // why\n/* how\n   more */ y = "s//t"; char c = \'*\';\n',
+                    '// x = 1;\n/* how\n   more */ y = "s//t"; char c = \'/\';\n'):
+        assert bench.canonical_source(changed) != bench.canonical_source(base), changed
+    assert '"s//t"' in bench.canonical_source(base)
+
+
 def test_traffic_record_follows_the_launch_plan(tmp_path, monkeypatch):
     # a record also holds the plan its counters were taken with: a table
     # change that gives the workload another launch makes it stale
